@@ -1,0 +1,396 @@
+"""Benchmark of the Ulysses attention block on GB300.
+
+One step = the whole hot path on one batch of the GPT-7B-like layer (B=1, L=32768, H=32,
+d_h=128, P=8 token shards, causal): attention forward with the seq->head relayout of
+Q, K, V fused into its loads and the head->seq relayout of O fused into its stores, then
+the backward with dO read and dQ, dK, dV written in the token-sharded layout. Inputs are
+seeded synthetic bf16 tensors resident in HBM before timing starts.
+
+Metric: attention fwd+bwd TFLOP/s over permitted (query, key) pairs only, 4*d_h flops per
+pair forward and 8*d_h backward (recompute not credited). The standalone relayout is
+timed beside it in HBM GB/s (2 bytes read + 2 written per element).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
+
+With --impl reference the CPU oracle is timed instead, on a bounded sample of rows.
+Under torchrun each rank runs its own replica (the path has no cross-rank exchange on
+one GPU); rank 0 prints one JSON line with the whole-job value.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "Ulysses attn fwd+bwd TFLOP/s & % BF16 peak; relayout HBM GB/s"
+
+
+def permitted_pairs(w: workloads.Workload) -> int:
+    """Permitted (query, key) pairs of one (batch, head)."""
+    if w.mask == "causal":
+        return w.L * (w.L + 1) // 2
+    if w.mask == "none":
+        return w.L * w.L
+    n = -(-w.L // w.tile)
+    qt = np.arange(n)[:, None]
+    kt = np.arange(n)[None, :]
+    act = ((kt >= qt - w.window_before) & (kt <= qt + w.window_after)) | (kt % w.global_stride == 0)
+    rows = np.minimum(w.tile, w.L - np.arange(n) * w.tile)
+    return int((act * rows[:, None] * rows[None, :]).sum())
+
+
+def flops(w: workloads.Workload, fwd_only: bool = False):
+    pairs = permitted_pairs(w) * w.B * w.H
+    f_fwd = 4 * w.d * pairs
+    f_bwd = 0 if (fwd_only or not w.backward) else 8 * w.d * pairs
+    return f_fwd, f_bwd
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops", 1900.0), d.get("hbm_gbs", 6800.0), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        if dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+
+def oracle_sample_step(w: workloads.Workload, t_bits, rows, heads):
+    """One oracle pass (forward + backward) on a bounded sample of rows and heads.
+    Returns the algorithmic flops of the sample."""
+    import oracle
+    mask = oracle.mask_for(w)
+    n_pairs = 0
+    for res in oracle.attention_sampled(t_bits["q"], t_bits["k"], t_bits["v"], t_bits["do"], w.P, mask, rows,
+                                        heads=heads):
+        allow = mask.rows(res["rows"], w.L)
+        n_pairs += int(allow.sum())
+    f = 4 * w.d * n_pairs + (8 * w.d * n_pairs if w.backward else 0)
+    return f
+
+
+def cpu_sample(w: workloads.Workload, n_rows: int, n_heads: int):
+    rows = workloads.sample_rows(w.B, w.L, n_rows, seed=w.seed + 100)
+    heads = list(range(0, w.H, max(1, w.H // n_heads)))[:n_heads]
+    return rows, heads
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    t = workloads.draw_workload(w)
+    bits = {n: workloads.to_bf16_bits(x) for n, x in t.items()}
+    rows, heads = cpu_sample(w, args.cpu_rows, args.cpu_heads)
+    for _ in range(args.warmup):
+        oracle_sample_step(w, bits, rows, heads)
+    t0 = time.perf_counter()
+    f = 0
+    for _ in range(args.steps):
+        f += oracle_sample_step(w, bits, rows, heads)
+    dt = time.perf_counter() - t0
+    value = f / dt / 1e12
+    sample = f"{len(rows)} sampled query rows x {len(heads)} heads of {w.name}, fwd+bwd, per step"
+    cores = os.cpu_count()
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "d_h": w.d, "P": w.P, "mask": w.mask},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def cuda_events_time(fn, stream, iters):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(iters):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / iters
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="gpt7b", choices=list(workloads.WORKLOADS))
+    ap.add_argument("--cpu-rows", type=int, default=64)
+    ap.add_argument("--cpu-heads", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = workloads.WORKLOADS[args.workload]
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, w, world, rank)
+
+    import ulysses_sequence_gb300 as U
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    f_fwd, f_bwd = flops(w)
+    total_flops = f_fwd + f_bwd
+
+    t = workloads.draw(w.B, w.L, w.H, w.d, w.P, w.seed + 1000 * rank, q_scale=w.q_scale)
+    host = {n: x.pin_memory() for n, x in t.items()}
+    x = {n: v.to(dev) for n, v in host.items()}
+    mask = U.Mask.causal() if w.mask == "causal" else (
+        U.Mask.none() if w.mask == "none" else
+        U.Mask.window_global(w.L, w.tile, w.window_before, w.window_after, w.global_stride, device=dev))
+    o = torch.empty_like(x["q"])
+    lse = torch.empty((w.P, w.B, w.Hp, w.L), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(3))
+    ws = U.bwd_workspace(x["q"], w.P)
+
+    def fwd():
+        U.attn_fwd(x["q"], x["k"], x["v"], w.P, mask, o=o, lse=lse)
+
+    def bwd():
+        U.attn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], w.P, mask, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    def step():
+        fwd()
+        if w.backward:
+            bwd()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, word = U.device_status()
+    U.check(st, f"device status after warm-up ({word:#x})")
+
+    # ---- timed region: K steps, device-resident inputs
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        if w.backward:
+            bwd()
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    st, word = U.device_status()
+    U.check(st, f"device status after timed steps ({word:#x})")
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    ms_per_step = elapsed_ms / args.steps
+    value = total_flops * world * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers (pinned)
+    host_out = {n: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for n, v in
+                (("o", o), ("dq", dq), ("dk", dk), ("dv", dv), ("lse", lse))}
+
+    def e2e_step():
+        for n in ("q", "k", "v", "do"):
+            x[n].copy_(host[n], non_blocking=True)
+        step()
+        for n, v in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv), ("lse", lse)):
+            host_out[n].copy_(v, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = cuda_events_time(e2e_step, stream, max(1, args.steps // 2))
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in ("q", "k", "v", "do"))
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    # ---- standalone relayout (seq->head of one tensor), HBM bound
+    heads = torch.empty((w.P, w.B, w.L, w.Hp, w.d), dtype=torch.bfloat16, device=dev)
+    relayout = lambda: U.seq_to_head(x["q"], w.P, out=heads)  # noqa: E731
+    for _ in range(3):
+        relayout()
+    rl_ms = cuda_events_time(relayout, stream, 20)
+    rl_bytes = 2 * x["q"].numel() * x["q"].element_size()
+    peak_tf, peak_gbs, peak_src = measured_peaks()
+
+    # ---- dominant launch group: the backward call (Delta prep + main + dQ convert)
+    bwd_avg = statistics.mean(bwd_ms) if w.backward else 0.0
+    fwd_avg = statistics.mean(fwd_ms)
+    if w.backward and bwd_avg >= fwd_avg:
+        dom_name, dom_flops, dom_ms = "attn_bwd (Delta prep + main + dQ convert)", f_bwd, bwd_avg
+    else:
+        dom_name, dom_flops, dom_ms = "attn_fwd", f_fwd, fwd_avg
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            import oracle
+            oracle.build()
+            bits = {n: workloads.to_bf16_bits(v) for n, v in t.items()}
+            rows, heads_s = cpu_sample(w, args.cpu_rows, args.cpu_heads)
+            t0 = time.perf_counter()
+            fc = oracle_sample_step(w, bits, rows, heads_s)
+            dt = time.perf_counter() - t0
+            cpu = {"value": fc / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                   "sample": f"{len(rows)} sampled query rows x {len(heads_s)} heads of {w.name}, fwd+bwd "
+                             f"({fc / 1e9:.1f} GFLOP in {dt:.1f} s)"}
+        except Exception as exc:  # the baseline must not hide the GPU line
+            cpu = {"value": None, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                   "sample": f"failed: {exc}"}
+
+    if rank == 0:
+        pairs = permitted_pairs(w)
+        comm = 4 * w.B * w.L * w.H * w.d * 2 // w.P
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "d_h": w.d, "P": w.P, "mask": w.mask,
+                       "passes": "fwd+bwd" if w.backward else "fwd", "layout": "token-sharded (relayouts fused)",
+                       "l2": "inputs larger than L2 (4 x %.0f MB bf16)" % (x["q"].numel() * 2 / 1e6),
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "frac_of_peak": value / world / peak_tf,
+            "fwd_ms": fwd_avg, "bwd_ms": bwd_avg,
+            "fwd_tflops": f_fwd / (fwd_avg * 1e-3) / 1e12,
+            "bwd_tflops": (f_bwd / (bwd_avg * 1e-3) / 1e12) if w.backward else None,
+            "fa_convention_tflops": (f_fwd + f_bwd * 10 / 8) * world * args.steps / (elapsed_ms * 1e-3) / 1e12,
+            "permitted_pairs_per_head": pairs,
+            "relayout": {"kernel": "seq_to_head (one tensor)", "gbs": rl_bytes / (rl_ms * 1e-3) / 1e9,
+                         "ms": rl_ms, "bytes": rl_bytes, "frac_of_measured_hbm": rl_bytes / (rl_ms * 1e-3) / 1e9 / peak_gbs},
+            "accounted_alltoall_bytes_per_rank": {"fwd": comm, "leaves_rank": comm * (w.P - 1) // w.P,
+                                                  "note": "4Nh/P in bf16 bytes, accounted, not measured over a link"},
+            "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak_tf,
+                         "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": None,
+                         "peak_source": f"{peak_src} bf16 dense (burst)"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": total_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps * (1 + (3 if w.backward else 0)),
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,167 @@
+/*
+ * ulysses.h -- C ABI of the GB300 (sm_103a) DeepSpeed-Ulysses attention block.
+ *
+ * The operations are those of one Transformer layer's attention under Ulysses sequence
+ * parallelism, as described in "DeepSpeed Ulysses: System Optimizations for Enabling
+ * Training of Extreme Long Sequence Transformer Models" (paper summary, section 3.2
+ * "Big-Picture Architecture" and section 3.4.1 "Data Partitioning and Layout
+ * Transformation"; pinyu.ai page "Ulysses Sequence Parallelism: A Temporary Change of
+ * Layout", section "One attention block, end to end"):
+ *   1. Q, K, V arrive as P token shards [B, L/P, H, d_h];
+ *   2. a sequence-to-head all-to-all gives each of P head groups the full sequence for
+ *      H/P heads, [B, L, H/P, d_h];
+ *   3. exact attention O_h = softmax(Q_h K_h^T / sqrt(d_h) + mask) V_h runs per head;
+ *   4. a head-to-sequence all-to-all returns O to [B, L/P, H, d_h].
+ * The P "ranks" are P shards of one allocation in one GPU's memory, so each all-to-all is
+ * an on-device permutation.
+ *
+ * Notation: Lp = L / P, Hp = H / P, global token s = r * Lp + t for shard r, local token
+ * t; head group g owns heads h = g * Hp + j.
+ *
+ * Layouts (all contiguous, row-major, element = bf16 unless stated):
+ *   ULYSSES_LAYOUT_TOKEN_SHARDED  [P][B][Lp][H][d_h]   (shard r = one rank's tensor)
+ *   ULYSSES_LAYOUT_HEAD_SHARDED   [P][B][L][Hp][d_h]   (group g = one rank's tensor)
+ *   log-sum-exp (fp32, natural log of the scaled scores)  [P][B][Hp][L]
+ *
+ * Conventions for every call below:
+ *   - Ownership: the caller allocates and owns every buffer. The library allocates no
+ *     device memory; its only state is a per-process error word on each device.
+ *   - Pointers are device pointers unless stated. `stream` is a cudaStream_t passed as
+ *     void* (NULL = the legacy default stream). Calls enqueue work and return without
+ *     synchronising; a launch failure returns ULYSSES_ERR_CUDA.
+ *   - Arguments are validated before any launch: bad sizes or null pointers give
+ *     ULYSSES_ERR_INVALID_ARG, buffers not 16-byte aligned give ULYSSES_ERR_MISALIGNED,
+ *     valid but unimplemented cases give ULYSSES_ERR_UNSUPPORTED. Nothing is launched
+ *     when a call fails.
+ *   - Sizes with B == 0 or L == 0 are valid and launch nothing.
+ *   - In-place operation is not supported; overlapping inputs and outputs are undefined
+ *     (identical base pointers are rejected).
+ *   - bf16 results are rounded to nearest-even from fp32. Relayouts move 16-bit patterns
+ *     unchanged, NaN payloads included.
+ *   - Every wait inside a kernel is bounded (about two seconds). A kernel that runs out
+ *     of time records the fact in the device error word and returns early; read it with
+ *     ulysses_get_device_status().
+ */
+#ifndef ULYSSES_H
+#define ULYSSES_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ULYSSES_OK = 0,
+    ULYSSES_ERR_INVALID_ARG = 1,
+    ULYSSES_ERR_UNSUPPORTED = 2,
+    ULYSSES_ERR_MISALIGNED = 3,
+    ULYSSES_ERR_CUDA = 4,
+    ULYSSES_ERR_DEVICE_TIMEOUT = 5
+} ulysses_status_t;
+
+typedef enum {
+    ULYSSES_LAYOUT_TOKEN_SHARDED = 0,
+    ULYSSES_LAYOUT_HEAD_SHARDED = 1
+} ulysses_layout_t;
+
+typedef enum {
+    ULYSSES_MASK_NONE = 0,          /* bidirectional: every (query, key) pair          */
+    ULYSSES_MASK_CAUSAL = 1,        /* key s' permitted for query s iff s' <= s         */
+    ULYSSES_MASK_BLOCK_SPARSE = 2   /* whole tile x tile blocks from the lists below    */
+} ulysses_mask_kind_t;
+
+/* Shape of one attention block: batch B, sequence L (the paper's N), H heads of width
+ * d_h, P shards. Requires H % P == 0 and L % P == 0 (the head cut and the token cut must
+ * be even; pinyu.ai page, "Head-count constraints"). */
+typedef struct {
+    int B, L, H, d_h, P;
+} ulysses_shape_t;
+
+/* Attention mask. For ULYSSES_MASK_BLOCK_SPARSE (a sparsity pattern applied locally after
+ * the all-to-all, paper summary section 3.4.5 "Attention-Agnostic Design"): tile must be
+ * 128; with n = ceil(L / 128) tiles,
+ *   q_rowptr[n + 1], q_kcols[nnz]  -- CSR: key tiles of each query tile, ascending;
+ *   k_colptr[n + 1], k_qrows[nnz]  -- CSC: query tiles of each key tile, ascending;
+ * all int32 device arrays describing the same pattern (ulysses_bsmask_build_window_global
+ * builds a consistent pair on the host). A permitted tile admits every pair inside it.
+ * The same pattern applies to every batch entry and head. Lists that disagree with each
+ * other give undefined results. Other kinds ignore these fields. */
+typedef struct {
+    int kind;
+    int tile;
+    const int32_t *q_rowptr;
+    const int32_t *q_kcols;
+    const int32_t *k_colptr;
+    const int32_t *k_qrows;
+    int nnz;
+} ulysses_mask_t;
+
+/* Sequence-to-head relayout (the first all-to-all; paper summary section 3.4.1, pinyu.ai
+ * page "Use the other independent axis"):
+ *   out[g][b][s][j][e] = in[s / Lp][b][s % Lp][g * Hp + j][e].
+ * in: TOKEN_SHARDED bf16 (any 16-bit type), out: HEAD_SHARDED, both B*L*H*d_h elements.
+ * Any d_h >= 1 is accepted; buffers need only 2-byte alignment. */
+int ulysses_seq_to_head(ulysses_shape_t shape, const void *in, void *out, void *stream);
+
+/* Head-to-sequence relayout (the second all-to-all, "After attention: the reverse
+ * transformation"), the inverse permutation:
+ *   out[r][b][t][h][e] = in[h / Hp][b][r * Lp + t][h % Hp][e]. */
+int ulysses_head_to_seq(ulysses_shape_t shape, const void *in, void *out, void *stream);
+
+/* Attention forward for every head group (paper summary section 3.4.1 "The challenge at
+ * the attention boundary", pinyu.ai page "The layout that saves memory breaks at
+ * attention"):  S = scale * Q K^T + mask,  O = softmax(S) V,  lse = ln sum exp(S).
+ * q, k, v, o: bf16 in io_layout; with TOKEN_SHARDED the two relayouts are fused into the
+ * kernel's loads and stores, so o comes back token-sharded. lse: fp32 [P][B][Hp][L].
+ * softmax_scale <= 0 selects 1/sqrt(d_h). A row with no permitted key gets O = 0 and
+ * lse = -inf.
+ * Supported: d_h in {64, 128}. TOKEN_SHARDED additionally needs Lp % 8 == 0. Any L >= 1
+ * otherwise (a last partial tile is masked). Pointers 16-byte aligned. */
+int ulysses_attn_fwd(ulysses_shape_t shape, const ulysses_mask_t *mask, float softmax_scale,
+                     int io_layout, const void *q, const void *k, const void *v,
+                     void *o, float *lse, void *stream);
+
+/* Bytes of device workspace ulysses_attn_bwd needs for this shape (an fp32 dQ
+ * accumulator and the per-row Delta = rowsum(dO * O)). */
+size_t ulysses_attn_bwd_workspace_size(ulysses_shape_t shape);
+
+/* Attention backward (the analytic gradient of the forward above; the pages do not write
+ * it out). With P = exp(S - lse) on permitted pairs, Delta = rowsum(dO * O):
+ *   dV = P^T dO,  dS = P * (dO V^T - Delta),  dQ = scale dS K,  dK = scale dS^T Q.
+ * q, k, v, o, dO, dq, dk, dv: bf16 in io_layout (TOKEN_SHARDED fuses the relayout of dO
+ * in and of dq, dk, dv out); lse as written by ulysses_attn_fwd. workspace: at least
+ * ulysses_attn_bwd_workspace_size(shape) bytes, 256-byte aligned, caller-owned, contents
+ * need not be initialised. dq accumulates in fp32 with atomic adds, so its bits may vary
+ * from run to run by fp32 rounding; dk and dv are deterministic. */
+int ulysses_attn_bwd(ulysses_shape_t shape, const ulysses_mask_t *mask, float softmax_scale,
+                     int io_layout, const void *q, const void *k, const void *v,
+                     const void *o, const float *lse, const void *dO,
+                     void *dq, void *dk, void *dv,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Host helper: the block-sparse pattern "sliding window plus strided global key tiles".
+ * Query tile qt gets key tiles max(0, qt - window_before) .. min(n - 1, qt + window_after)
+ * and every kt with kt % global_stride == 0 (global_stride <= 0: none), n = ceil(L/tile).
+ * Writes host arrays rowptr[n + 1], kcols[cap], colptr[n + 1], qrows[cap]; *nnz holds the
+ * capacity on entry and the number of active tiles on return. Returns INVALID_ARG if the
+ * capacity is too small (*nnz then holds the size needed) or arguments are bad. */
+int ulysses_bsmask_build_window_global(int L, int tile, int window_before, int window_after,
+                                       int global_stride, int32_t *rowptr, int32_t *kcols,
+                                       int32_t *colptr, int32_t *qrows, int *nnz);
+
+/* Synchronises `stream`, then reads and clears the current device's error word.
+ * Returns ULYSSES_OK, ULYSSES_ERR_DEVICE_TIMEOUT (a bounded wait ran out), or
+ * ULYSSES_ERR_CUDA. When detail is not NULL it receives the raw word (kernel, role and
+ * wait site of the first failure). */
+int ulysses_get_device_status(void *stream, uint32_t *detail);
+
+/* Human-readable name of a status code (static storage). */
+const char *ulysses_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ULYSSES_H */

@@ -1,0 +1,222 @@
+"""GPU parity of the attention forward and backward (through the C ABI) against the fp64
+oracle: every row at small sizes (several tiles, ragged tails, B > 1, both layouts, all
+mask kinds, an empty query tile), every row of the GPT-1.2B-like forward, and sampled rows
+of the three large workloads; plus properties that hold at any size (results do not depend
+on the shard count P or on fusing the relayouts, dK/dV are deterministic)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ulysses_sequence_gb300 as U
+import workloads
+from gpu_util import (ErrStats, LSE_MAX_ABS, env_rows, f64, gpu_mask, logical, lse_logical, need_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def oracle_mask(kind, L, tiles=None, w=None):
+    if kind in ("causal", "none"):
+        return oracle.Mask(kind)
+    if w is not None:
+        return oracle.mask_for(w)
+    return oracle.Mask("tiles", 128, tiles)
+
+
+def run_case(B, L, H, d, P, kind, layout, seed, tiles=None, backward=True):
+    t = workloads.draw(B, L, H, d, P, seed)
+    bits = {n: workloads.to_bf16_bits(x) for n, x in t.items()}
+    ref = oracle.attention_full(bits["q"], bits["k"], bits["v"], P, oracle_mask(kind, L, tiles),
+                                do_tok=bits["do"] if backward else None)
+    if layout == U.LAYOUT_HEAD_SHARDED:
+        dev = {n: torch.from_numpy(oracle.seq_to_head(b, P).view(np.int16)).view(torch.bfloat16).cuda()
+               for n, b in bits.items()}
+    else:
+        dev = {n: x.cuda() for n, x in t.items()}
+    mask = gpu_mask(kind, L, tiles)
+    o, lse = U.attn_fwd(dev["q"], dev["k"], dev["v"], P, mask, layout)
+    outs = {"o": o}
+    if backward:
+        dq, dk, dv = U.attn_bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], P, mask, layout)
+        outs.update(dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    st, word = U.device_status()
+    assert st == U.OK, hex(word)
+    got = {}
+    for n, x in outs.items():
+        bits_out = x.cpu().view(torch.int16).numpy().view(np.uint16)
+        if layout == U.LAYOUT_HEAD_SHARDED:
+            bits_out = oracle.head_to_seq(bits_out, P)
+        got[n] = oracle.bf16_to_f64(bits_out)
+    got["lse"] = lse.cpu().double().numpy()
+    return got, ref
+
+
+def check_all(got, ref, backward=True):
+    for n in (["o", "dq", "dk", "dv"] if backward else ["o"]):
+        s = ErrStats(n)
+        s.add(got[n], ref[n])
+        s.check()
+    lg, lr = got["lse"], ref["lse"]
+    assert np.array_equal(np.isneginf(lg), np.isneginf(lr))
+    fin = np.isfinite(lr)
+    assert np.abs(lg[fin] - lr[fin]).max() <= LSE_MAX_ABS
+
+
+CASES = [
+    # name, B, L, H, d, P, mask, layout
+    ("tiny", 1, 256, 8, 64, 4, "causal", U.LAYOUT_TOKEN_SHARDED),
+    ("b2_d128_causal", 2, 384, 4, 128, 2, "causal", U.LAYOUT_TOKEN_SHARDED),
+    ("ragged_token", 1, 320, 4, 128, 4, "causal", U.LAYOUT_TOKEN_SHARDED),
+    ("ragged_head_dense", 1, 300, 6, 64, 3, "none", U.LAYOUT_HEAD_SHARDED),
+    ("dense_p1", 1, 512, 2, 128, 1, "none", U.LAYOUT_TOKEN_SHARDED),
+    ("head_layout_causal", 2, 256, 4, 128, 4, "causal", U.LAYOUT_HEAD_SHARDED),
+]
+
+
+@pytest.mark.parametrize("name,B,L,H,d,P,kind,layout", CASES, ids=[c[0] for c in CASES])
+def test_attention_small_full(name, B, L, H, d, P, kind, layout):
+    got, ref = run_case(B, L, H, d, P, kind, layout, seed=sum(map(ord, name)))
+    check_all(got, ref)
+
+
+@pytest.mark.parametrize("layout", [U.LAYOUT_TOKEN_SHARDED, U.LAYOUT_HEAD_SHARDED])
+def test_attention_block_sparse_small(layout):
+    L = 1024
+    tiles = oracle.window_global_tiles(L // 128, 1, 1, 4)
+    got, ref = run_case(2, L, 4, 128, 4, "tiles", layout, seed=11, tiles=tiles)
+    check_all(got, ref)
+
+
+def test_attention_block_sparse_empty_query_tile():
+    """A query tile with no key tile: O = 0, lse = -inf, dQ = 0 there, finite elsewhere."""
+    L = 640
+    tiles = oracle.window_global_tiles(L // 128, 1, 0, 3).copy()
+    tiles[2, :] = False
+    got, ref = run_case(1, L, 4, 128, 2, "tiles", U.LAYOUT_TOKEN_SHARDED, seed=12, tiles=tiles)
+    check_all(got, ref)
+    assert np.all(logical(got["o"])[:, 256:384] == 0)
+    assert np.all(logical(got["dq"])[:, 256:384] == 0)
+
+
+def test_tiny_workload():
+    w = workloads.WORKLOADS["tiny"]
+    t = workloads.draw_workload(w)
+    bits = {n: workloads.to_bf16_bits(x) for n, x in t.items()}
+    ref = oracle.attention_full(bits["q"], bits["k"], bits["v"], w.P, oracle.mask_for(w), do_tok=bits["do"])
+    dev = {n: x.cuda() for n, x in t.items()}
+    o, lse = U.attn_fwd(dev["q"], dev["k"], dev["v"], w.P, U.Mask.causal())
+    dq, dk, dv = U.attn_bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], w.P, U.Mask.causal())
+    got = {"o": f64(o), "dq": f64(dq), "dk": f64(dk), "dv": f64(dv), "lse": lse.cpu().double().numpy()}
+    check_all(got, ref)
+
+
+def test_shard_count_and_fusion_do_not_change_results():
+    """Per-head attention does not depend on P, nor on reading through the token layout
+    instead of relayouting first: forward outputs and dK, dV must be bit-identical."""
+    B, L, H, d = 1, 512, 8, 128
+    g = torch.Generator().manual_seed(7)
+    x = {n: torch.randn((B, L, H, d), generator=g).to(torch.bfloat16) for n in ("q", "k", "v", "do")}
+    base = None
+    for P in (1, 2, 4, 8):
+        tok = {n: workloads.shard_tokens(t, P).cuda() for n, t in x.items()}
+        for layout in (U.LAYOUT_TOKEN_SHARDED, U.LAYOUT_HEAD_SHARDED):
+            ins = tok if layout == U.LAYOUT_TOKEN_SHARDED else {n: U.seq_to_head(t, P) for n, t in tok.items()}
+            o, lse = U.attn_fwd(ins["q"], ins["k"], ins["v"], P, U.Mask.causal(), layout)
+            dq, dk, dv = U.attn_bwd(ins["q"], ins["k"], ins["v"], o, lse, ins["do"], P, U.Mask.causal(), layout)
+            if layout == U.LAYOUT_HEAD_SHARDED:
+                o, dq, dk, dv = (U.head_to_seq(t, P) for t in (o, dq, dk, dv))
+            res = {n: t.cpu().permute(1, 0, 2, 3, 4).reshape(B, L, H, d) for n, t in
+                   (("o", o), ("dq", dq), ("dk", dk), ("dv", dv))}
+            res["lse"] = lse.cpu().permute(1, 0, 2, 3).reshape(B, H, L)
+            if base is None:
+                base = res
+                continue
+            for n in ("o", "lse", "dk", "dv"):
+                assert torch.equal(res[n].view(torch.int16) if res[n].dtype == torch.bfloat16 else res[n],
+                                   base[n].view(torch.int16) if base[n].dtype == torch.bfloat16 else base[n]), (P, layout, n)
+            err = (res["dq"].float() - base["dq"].float()).abs().max().item()
+            assert err <= 2e-2, (P, layout, err)
+
+
+def test_repeat_runs_are_deterministic_except_dq():
+    w = workloads.Workload("rep", 1, 1024, 4, 128, 4, "causal", True, 5)
+    t = {n: x.cuda() for n, x in workloads.draw_workload(w).items()}
+    runs = []
+    for _ in range(3):
+        o, lse = U.attn_fwd(t["q"], t["k"], t["v"], w.P, U.Mask.causal())
+        dq, dk, dv = U.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], w.P, U.Mask.causal())
+        runs.append([x.clone() for x in (o, lse, dk, dv)])
+    for r in runs[1:]:
+        for a, b in zip(r, runs[0]):
+            assert torch.equal(a, b)
+
+
+def test_gpt1p2b_forward_every_row():
+    w = workloads.WORKLOADS["gpt1.2b"]
+    t = workloads.draw_workload(w, names=("q", "k", "v"))
+    bits = {n: workloads.to_bf16_bits(x) for n, x in t.items()}
+    dev = {n: x.cuda() for n, x in t.items()}
+    o, lse = U.attn_fwd(dev["q"], dev["k"], dev["v"], w.P, U.Mask.causal())
+    torch.cuda.synchronize()
+    ref = oracle.attention_full(bits["q"], bits["k"], bits["v"], w.P, oracle.mask_for(w))
+    check_all({"o": f64(o), "lse": lse.cpu().double().numpy()}, ref, backward=False)
+
+
+SAMPLED = [("gpt7b", None), ("long", (0, 9, 18, 31)), ("block_sparse", None)]
+
+
+@pytest.mark.parametrize("name,heads", SAMPLED, ids=[s[0] for s in SAMPLED])
+def test_large_workload_sampled_rows(name, heads):
+    """4096 seeded query rows: O, lse and dQ of those rows from a pass with the full dO
+    (run A), and dK, dV over every key from a pass whose dO is zero outside those rows
+    (run B), which then hold exactly the sampled rows' gradient contributions."""
+    w = workloads.WORKLOADS[name]
+    t = workloads.draw_workload(w)
+    P, B, L, H, d = w.P, w.B, w.L, w.H, w.d
+    rows = workloads.sample_rows(B, L, env_rows(w.sampled_rows), seed=w.seed)
+    keep = torch.zeros((B, L), dtype=torch.bool)
+    keep[torch.from_numpy(rows[:, 0]), torch.from_numpy(rows[:, 1])] = True
+    keep_tok = keep.reshape(B, P, L // P).permute(1, 0, 2)[..., None, None]
+    dev = {n: x.cuda() for n, x in t.items()}
+    mask = gpu_mask(w.mask, L, w=w) if w.mask == "block_sparse" else gpu_mask(w.mask, L)
+    o, lse = U.attn_fwd(dev["q"], dev["k"], dev["v"], P, mask)
+    dqA, _, _ = U.attn_bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], P, mask)
+    do_b = dev["do"] * keep_tok.cuda().to(torch.bfloat16)
+    dqB, dkB, dvB = U.attn_bwd(dev["q"], dev["k"], dev["v"], o, lse, do_b, P, mask)
+    torch.cuda.synchronize()
+    st, word = U.device_status()
+    assert st == U.OK, hex(word)
+
+    def logical_t(x):
+        return x.cpu().permute(1, 0, 2, 3, 4).reshape(B, L, H, d)
+
+    O, dQA, dQB, dKB, dVB = (logical_t(x) for x in (o, dqA, dqB, dkB, dvB))
+    LSE = lse.cpu().permute(1, 0, 2, 3).reshape(B, H, L)
+    # rows outside the sample get no dQ in run B
+    assert torch.count_nonzero(dQB.float()[~keep]) == 0
+    del dev, o, dqA, dqB, dkB, dvB, do_b
+    torch.cuda.empty_cache()
+
+    stats = {n: ErrStats(n) for n in ("o", "dq", "dk", "dv")}
+    lse_err = 0.0
+    bits = {n: workloads.to_bf16_bits(x) for n, x in t.items()}
+    for res in oracle.attention_sampled(bits["q"], bits["k"], bits["v"], bits["do"], P, oracle.mask_for(w), rows,
+                                        heads=heads):
+        b, h, r = res["b"], res["h"], torch.from_numpy(res["rows"])
+        stats["o"].add(O[b, r, h].double().numpy(), res["o"])
+        stats["dq"].add(dQA[b, r, h].double().numpy(), res["dq"])
+        stats["dk"].add(dKB[b, :, h].double().numpy(), res["dk"])
+        stats["dv"].add(dVB[b, :, h].double().numpy(), res["dv"])
+        lse_err = max(lse_err, float(np.abs(LSE[b, h, r].double().numpy() - res["lse"]).max()))
+    for s in stats.values():
+        s.check()
+    assert lse_err <= LSE_MAX_ABS, lse_err

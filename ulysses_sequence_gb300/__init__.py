@@ -1,0 +1,261 @@
+"""GB300 (sm_103a) DeepSpeed-Ulysses attention block: Python binding of libulysses.so.
+
+The functions named ``ulysses_*`` are the C ABI of ``include/ulysses.h`` one for one
+(ctypes, plain integers for pointers and streams). The snake-case helpers below them take
+torch CUDA tensors and only marshal pointers, shapes and the current stream into those
+calls; every step of the computation runs in the library's CUDA kernels. PyTorch provides
+device memory and streams only.
+
+There is no fallback: if libulysses.so has not been built (``python -m
+ulysses_sequence_gb300.build`` or ``__graft_entry__.build()``), loading raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libulysses.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_DEVICE_TIMEOUT = range(6)
+LAYOUT_TOKEN_SHARDED, LAYOUT_HEAD_SHARDED = 0, 1
+MASK_NONE, MASK_CAUSAL, MASK_BLOCK_SPARSE = 0, 1, 2
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("L", ctypes.c_int), ("H", ctypes.c_int), ("d_h", ctypes.c_int),
+                ("P", ctypes.c_int)]
+
+
+class MaskStruct(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("tile", ctypes.c_int), ("q_rowptr", ctypes.c_void_p),
+                ("q_kcols", ctypes.c_void_p), ("k_colptr", ctypes.c_void_p), ("k_qrows", ctypes.c_void_p),
+                ("nnz", ctypes.c_int)]
+
+
+EXPORTS = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_attn_fwd", "ulysses_attn_bwd_workspace_size",
+           "ulysses_attn_bwd", "ulysses_bsmask_build_window_global", "ulysses_get_device_status",
+           "ulysses_status_string")
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libulysses.so from this package directory (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m ulysses_sequence_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.ulysses_seq_to_head.argtypes = [Shape, vp, vp, vp]
+    lib.ulysses_head_to_seq.argtypes = [Shape, vp, vp, vp]
+    lib.ulysses_attn_fwd.argtypes = [Shape, ctypes.POINTER(MaskStruct), f, i, vp, vp, vp, vp, vp, vp]
+    lib.ulysses_attn_bwd_workspace_size.argtypes = [Shape]
+    lib.ulysses_attn_bwd_workspace_size.restype = sz
+    lib.ulysses_attn_bwd.argtypes = [Shape, ctypes.POINTER(MaskStruct), f, i, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                     vp, sz, vp]
+    ip = ctypes.POINTER(ctypes.c_int32)
+    lib.ulysses_bsmask_build_window_global.argtypes = [i, i, i, i, i, ip, ip, ip, ip, ctypes.POINTER(ctypes.c_int)]
+    lib.ulysses_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.ulysses_status_string.argtypes = [i]
+    lib.ulysses_status_string.restype = ctypes.c_char_p
+    for name in EXPORTS:
+        if name != "ulysses_attn_bwd_workspace_size" and name != "ulysses_status_string":
+            getattr(lib, name).restype = i
+    _lib = lib
+    return lib
+
+
+# ----------------------------------------------------------------------------- raw C ABI
+
+def _mref(mask):
+    return None if mask is None else ctypes.byref(mask)
+
+
+def ulysses_seq_to_head(shape: Shape, inp: int, out: int, stream: int) -> int:
+    return load().ulysses_seq_to_head(shape, inp, out, stream)
+
+
+def ulysses_head_to_seq(shape: Shape, inp: int, out: int, stream: int) -> int:
+    return load().ulysses_head_to_seq(shape, inp, out, stream)
+
+
+def ulysses_attn_fwd(shape: Shape, mask: MaskStruct, softmax_scale: float, io_layout: int, q: int, k: int, v: int,
+                     o: int, lse: int, stream: int) -> int:
+    return load().ulysses_attn_fwd(shape, _mref(mask), softmax_scale, io_layout, q, k, v, o, lse, stream)
+
+
+def ulysses_attn_bwd_workspace_size(shape: Shape) -> int:
+    return load().ulysses_attn_bwd_workspace_size(shape)
+
+
+def ulysses_attn_bwd(shape: Shape, mask: MaskStruct, softmax_scale: float, io_layout: int, q: int, k: int, v: int,
+                     o: int, lse: int, dO: int, dq: int, dk: int, dv: int, workspace: int, workspace_bytes: int,
+                     stream: int) -> int:
+    return load().ulysses_attn_bwd(shape, _mref(mask), softmax_scale, io_layout, q, k, v, o, lse, dO, dq, dk,
+                                   dv, workspace, workspace_bytes, stream)
+
+
+def ulysses_bsmask_build_window_global(L: int, tile: int, window_before: int, window_after: int,
+                                       global_stride: int):
+    """Returns host lists (rowptr, kcols, colptr, qrows) built by the library."""
+    lib = load()
+    n = (L + tile - 1) // tile
+    nnz = ctypes.c_int(0)
+    rp = (ctypes.c_int32 * (n + 1))()
+    cp = (ctypes.c_int32 * (n + 1))()
+    lib.ulysses_bsmask_build_window_global(L, tile, window_before, window_after, global_stride, rp, None, cp, None,
+                                           ctypes.byref(nnz))
+    cap = nnz.value
+    kc = (ctypes.c_int32 * max(cap, 1))()
+    qr = (ctypes.c_int32 * max(cap, 1))()
+    nnz = ctypes.c_int(cap)
+    rc = lib.ulysses_bsmask_build_window_global(L, tile, window_before, window_after, global_stride, rp, kc, cp, qr,
+                                                ctypes.byref(nnz))
+    check(rc, "ulysses_bsmask_build_window_global")
+    return list(rp), list(kc)[:cap], list(cp), list(qr)[:cap]
+
+
+def ulysses_get_device_status(stream: int) -> Tuple[int, int]:
+    detail = ctypes.c_uint32(0)
+    rc = load().ulysses_get_device_status(stream, ctypes.byref(detail))
+    return rc, detail.value
+
+
+def ulysses_status_string(status: int) -> str:
+    return load().ulysses_status_string(status).decode()
+
+
+class UlyssesError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {ulysses_status_string(status)}")
+        self.status = status
+
+
+def check(status: int, where: str) -> None:
+    if status != OK:
+        raise UlyssesError(status, where)
+
+
+# ----------------------------------------------------------------------------- torch helpers
+
+def _stream(stream) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def token_shape(x, P: int) -> Shape:
+    """Shape of a token-sharded tensor [P][B][Lp][H][d]."""
+    P_, B, Lp, H, d = x.shape
+    assert P_ == P, "leading dimension must be the shard count P"
+    return Shape(B, Lp * P, H, d, P)
+
+
+def head_shape(y, P: int) -> Shape:
+    """Shape of a head-sharded tensor [P][B][L][Hp][d]."""
+    P_, B, L, Hp, d = y.shape
+    assert P_ == P, "leading dimension must be the shard count P"
+    return Shape(B, L, Hp * P, d, P)
+
+
+class Mask:
+    """An attention mask for the C ABI; for block-sparse masks it owns the device tile lists."""
+
+    def __init__(self, kind: int, tile: int = 128, lists=None):
+        self.kind, self.tile, self.lists = kind, tile, lists
+        self.struct = MaskStruct(kind, tile, None, None, None, None, 0)
+        if lists is not None:
+            rp, kc, cp, qr = lists
+            self.struct = MaskStruct(kind, tile, rp.data_ptr(), kc.data_ptr(), cp.data_ptr(), qr.data_ptr(),
+                                     int(kc.numel()))
+
+    @staticmethod
+    def causal() -> "Mask":
+        return Mask(MASK_CAUSAL)
+
+    @staticmethod
+    def none() -> "Mask":
+        return Mask(MASK_NONE)
+
+    @staticmethod
+    def window_global(L: int, tile: int = 128, window_before: int = 4, window_after: int = 3,
+                      global_stride: int = 16, device="cuda") -> "Mask":
+        import torch
+        rp, kc, cp, qr = ulysses_bsmask_build_window_global(L, tile, window_before, window_after, global_stride)
+        t = [torch.tensor(x if x else [0], dtype=torch.int32, device=device) for x in (rp, kc, cp, qr)]
+        return Mask(MASK_BLOCK_SPARSE, tile, t)
+
+    @staticmethod
+    def from_tile_lists(rowptr, kcols, colptr, qrows, tile: int = 128, device="cuda") -> "Mask":
+        import torch
+        t = [torch.as_tensor(x, dtype=torch.int32).to(device) for x in (rowptr, kcols, colptr, qrows)]
+        return Mask(MASK_BLOCK_SPARSE, tile, t)
+
+
+def seq_to_head(x, P: int, out=None, stream=None):
+    """[P][B][Lp][H][d] -> [P][B][L][Hp][d] on the GPU (16-bit elements)."""
+    import torch
+    Pn, B, Lp, H, d = x.shape
+    if out is None:
+        out = torch.empty((P, B, Lp * P, H // P, d), dtype=x.dtype, device=x.device)
+    check(ulysses_seq_to_head(token_shape(x, P), x.data_ptr(), out.data_ptr(), _stream(stream)), "seq_to_head")
+    return out
+
+
+def head_to_seq(y, P: int, out=None, stream=None):
+    """[P][B][L][Hp][d] -> [P][B][Lp][H][d] on the GPU (16-bit elements)."""
+    import torch
+    Pn, B, L, Hp, d = y.shape
+    if out is None:
+        out = torch.empty((P, B, L // P, Hp * P, d), dtype=y.dtype, device=y.device)
+    check(ulysses_head_to_seq(head_shape(y, P), y.data_ptr(), out.data_ptr(), _stream(stream)), "head_to_seq")
+    return out
+
+
+def _shape_of(x, P: int, layout: int) -> Shape:
+    return token_shape(x, P) if layout == LAYOUT_TOKEN_SHARDED else head_shape(x, P)
+
+
+def attn_fwd(q, k, v, P: int, mask: Mask, layout: int = LAYOUT_TOKEN_SHARDED, scale: float = 0.0, o=None,
+             lse=None, stream=None):
+    """Attention forward through ulysses_attn_fwd. Returns (o, lse[P][B][Hp][L] fp32)."""
+    import torch
+    shape = _shape_of(q, P, layout)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((P, shape.B, shape.H // P, shape.L), dtype=torch.float32, device=q.device)
+    check(ulysses_attn_fwd(shape, mask.struct, scale, layout, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr(), _stream(stream)), "attn_fwd")
+    return o, lse
+
+
+def bwd_workspace(q, P: int, layout: int = LAYOUT_TOKEN_SHARDED):
+    import torch
+    n = ulysses_attn_bwd_workspace_size(_shape_of(q, P, layout))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+
+
+def attn_bwd(q, k, v, o, lse, do, P: int, mask: Mask, layout: int = LAYOUT_TOKEN_SHARDED, scale: float = 0.0,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Attention backward through ulysses_attn_bwd. Returns (dq, dk, dv)."""
+    import torch
+    shape = _shape_of(q, P, layout)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = bwd_workspace(q, P, layout) if workspace is None else workspace
+    check(ulysses_attn_bwd(shape, mask.struct, scale, layout, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
+                           ws.numel(), _stream(stream)), "attn_bwd")
+    return dq, dk, dv
+
+
+def device_status(stream=None) -> Tuple[int, int]:
+    """Synchronises the stream and reads/clears the device error word: (status, raw word)."""
+    return ulysses_get_device_status(_stream(stream))

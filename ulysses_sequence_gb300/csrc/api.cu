@@ -1,0 +1,259 @@
+// Host side of the C ABI declared in include/ulysses.h: argument validation, tensor-map
+// encoding, the per-device error word and the block-sparse tile-list builder.
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "ulysses_internal.h"
+
+namespace ulysses {
+
+// The per-process error word of each device that loads this library (4 bytes).
+__device__ uint32_t g_error_word_storage;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sms[kMaxDevices] = {};
+uint32_t* g_err[kMaxDevices] = {};
+// signature of cuTensorMapEncodeTiled (driver API), looked up at run time
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+
+bool load_encode_fn() {
+    if (g_encode) return true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+int device_sm_count() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 148;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
+uint32_t* device_error_word() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_error_word_storage) != cudaSuccess) return nullptr;
+        g_err[dev] = static_cast<uint32_t*>(ptr);
+    }
+    return g_err[dev];
+}
+
+bool encode_qkv_map(CUtensorMap* map, const void* base, const ulysses_shape_t& s, int layout, int box_rows) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!load_encode_fn()) return false;
+    }
+    const uint64_t d = s.d_h, H = s.H, P = s.P, B = s.B, L = s.L;
+    const uint64_t Hp = H / P, Lp = L / P;
+    cuuint64_t dims[5];
+    cuuint64_t strides[4];  // bytes, dims 1..4
+    if (layout == ULYSSES_LAYOUT_TOKEN_SHARDED) {
+        dims[0] = d; dims[1] = H; dims[2] = Lp; dims[3] = B; dims[4] = P;
+    } else {
+        dims[0] = d; dims[1] = Hp; dims[2] = L; dims[3] = B; dims[4] = P;
+    }
+    strides[0] = dims[0] * 2;
+    strides[1] = strides[0] * dims[1];
+    strides[2] = strides[1] * dims[2];
+    strides[3] = strides[2] * dims[3];
+    cuuint32_t box[5] = {64, 1, static_cast<cuuint32_t>(box_rows), 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+int validate_shape(const ulysses_shape_t& s) {
+    if (s.B < 0 || s.L < 0 || s.H <= 0 || s.d_h <= 0 || s.P <= 0) return ULYSSES_ERR_INVALID_ARG;
+    if (s.H % s.P != 0 || s.L % s.P != 0) return ULYSSES_ERR_INVALID_ARG;
+    // element counts must fit the kernels' 64-bit offsets and 32-bit row counters
+    if (uint64_t(s.B) * uint64_t(s.L) * uint64_t(s.H) * uint64_t(s.d_h) > (1ull << 40)) return ULYSSES_ERR_INVALID_ARG;
+    return ULYSSES_OK;
+}
+
+int validate_attn(const ulysses_shape_t& s, const ulysses_mask_t* mask, int layout) {
+    int rc = validate_shape(s);
+    if (rc != ULYSSES_OK) return rc;
+    if (!mask) return ULYSSES_ERR_INVALID_ARG;
+    if (mask->kind != ULYSSES_MASK_NONE && mask->kind != ULYSSES_MASK_CAUSAL && mask->kind != ULYSSES_MASK_BLOCK_SPARSE)
+        return ULYSSES_ERR_INVALID_ARG;
+    if (layout != ULYSSES_LAYOUT_TOKEN_SHARDED && layout != ULYSSES_LAYOUT_HEAD_SHARDED) return ULYSSES_ERR_INVALID_ARG;
+    if (mask->kind == ULYSSES_MASK_BLOCK_SPARSE) {
+        if (mask->tile != kTile) return ULYSSES_ERR_UNSUPPORTED;
+        if (!mask->q_rowptr || !mask->q_kcols || !mask->k_colptr || !mask->k_qrows || mask->nnz < 0)
+            return ULYSSES_ERR_INVALID_ARG;
+    }
+    if (s.d_h != 64 && s.d_h != 128) return ULYSSES_ERR_UNSUPPORTED;
+    if (layout == ULYSSES_LAYOUT_TOKEN_SHARDED && (s.L / s.P) % 8 != 0 && s.L > 0) return ULYSSES_ERR_UNSUPPORTED;
+    // grid limits: B*H CTAs along x, ceil(L / 128) along y
+    if (uint64_t(s.B) * s.H > 0x7fffffffull || (uint64_t(s.L) + kTile - 1) / kTile > 65535) return ULYSSES_ERR_UNSUPPORTED;
+    return ULYSSES_OK;
+}
+
+float resolve_scale(float scale, int d) { return scale > 0.f ? scale : 1.0f / sqrtf(float(d)); }
+
+}  // namespace
+}  // namespace ulysses
+
+using namespace ulysses;
+
+extern "C" {
+
+const char* ulysses_status_string(int status) {
+    switch (status) {
+        case ULYSSES_OK: return "ULYSSES_OK";
+        case ULYSSES_ERR_INVALID_ARG: return "ULYSSES_ERR_INVALID_ARG";
+        case ULYSSES_ERR_UNSUPPORTED: return "ULYSSES_ERR_UNSUPPORTED";
+        case ULYSSES_ERR_MISALIGNED: return "ULYSSES_ERR_MISALIGNED";
+        case ULYSSES_ERR_CUDA: return "ULYSSES_ERR_CUDA";
+        case ULYSSES_ERR_DEVICE_TIMEOUT: return "ULYSSES_ERR_DEVICE_TIMEOUT";
+        default: return "ULYSSES_ERR_UNKNOWN";
+    }
+}
+
+static int relayout_common(ulysses_shape_t shape, const void* in, void* out, void* stream, bool to_head) {
+    int rc = validate_shape(shape);
+    if (rc != ULYSSES_OK) return rc;
+    const uint64_t n = uint64_t(shape.B) * shape.L * shape.H * shape.d_h;
+    if (n == 0) return ULYSSES_OK;
+    if (!in || !out) return ULYSSES_ERR_INVALID_ARG;
+    if (in == out) return ULYSSES_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 1u) return ULYSSES_ERR_MISALIGNED;
+    return launch_relayout(shape, in, out, static_cast<cudaStream_t>(stream), to_head);
+}
+
+int ulysses_seq_to_head(ulysses_shape_t shape, const void* in, void* out, void* stream) {
+    return relayout_common(shape, in, out, stream, true);
+}
+
+int ulysses_head_to_seq(ulysses_shape_t shape, const void* in, void* out, void* stream) {
+    return relayout_common(shape, in, out, stream, false);
+}
+
+int ulysses_attn_fwd(ulysses_shape_t shape, const ulysses_mask_t* mask, float softmax_scale, int io_layout,
+                     const void* q, const void* k, const void* v, void* o, float* lse, void* stream) {
+    int rc = validate_attn(shape, mask, io_layout);
+    if (rc != ULYSSES_OK) return rc;
+    if (shape.B == 0 || shape.L == 0) return ULYSSES_OK;
+    if (!q || !k || !v || !o || !lse) return ULYSSES_ERR_INVALID_ARG;
+    if (o == q || o == k || o == v) return ULYSSES_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ULYSSES_ERR_MISALIGNED;
+    MaskArgs m{mask->kind, mask->q_rowptr, mask->q_kcols, mask->k_colptr, mask->k_qrows};
+    return launch_attn_fwd(shape, m, resolve_scale(softmax_scale, shape.d_h), io_layout, q, k, v, o, lse,
+                           static_cast<cudaStream_t>(stream));
+}
+
+size_t ulysses_attn_bwd_workspace_size(ulysses_shape_t shape) {
+    if (validate_shape(shape) != ULYSSES_OK) return 0;
+    return bwd_workspace_bytes(shape);
+}
+
+int ulysses_attn_bwd(ulysses_shape_t shape, const ulysses_mask_t* mask, float softmax_scale, int io_layout,
+                     const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                     void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = validate_attn(shape, mask, io_layout);
+    if (rc != ULYSSES_OK) return rc;
+    if (shape.B == 0 || shape.L == 0) return ULYSSES_OK;
+    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace) return ULYSSES_ERR_INVALID_ARG;
+    if (workspace_bytes < bwd_workspace_bytes(shape)) return ULYSSES_ERR_INVALID_ARG;
+    const void* ins[] = {q, k, v, o, lse, dO};
+    const void* outs[] = {dq, dk, dv, workspace};
+    for (const void* a : outs)
+        for (const void* b : ins)
+            if (a == b) return ULYSSES_ERR_INVALID_ARG;
+    if (dq == dk || dq == dv || dk == dv) return ULYSSES_ERR_INVALID_ARG;
+    for (const void* a : ins)
+        if (!aligned16(a)) return ULYSSES_ERR_MISALIGNED;
+    for (const void* a : outs)
+        if (!aligned16(a)) return ULYSSES_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ULYSSES_ERR_MISALIGNED;
+    MaskArgs m{mask->kind, mask->q_rowptr, mask->q_kcols, mask->k_colptr, mask->k_qrows};
+    return launch_attn_bwd(shape, m, resolve_scale(softmax_scale, shape.d_h), io_layout, q, k, v, o, lse, dO, dq, dk,
+                           dv, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int ulysses_bsmask_build_window_global(int L, int tile, int window_before, int window_after, int global_stride,
+                                       int32_t* rowptr, int32_t* kcols, int32_t* colptr, int32_t* qrows, int* nnz) {
+    if (L <= 0 || tile <= 0 || window_before < 0 || window_after < 0 || !nnz || !rowptr || !colptr)
+        return ULYSSES_ERR_INVALID_ARG;
+    const int n = (L + tile - 1) / tile;
+    // pass 1: count, building CSR; a key tile is active for query tile qt if it lies in the
+    // window [qt - window_before, qt + window_after] or is a global tile
+    std::vector<int32_t> rp(n + 1, 0), cols;
+    cols.reserve(size_t(n) * (window_before + window_after + 1 + (global_stride > 0 ? n / global_stride + 1 : 0)));
+    for (int qt = 0; qt < n; ++qt) {
+        const int lo = qt - window_before < 0 ? 0 : qt - window_before;
+        const int hi = qt + window_after > n - 1 ? n - 1 : qt + window_after;
+        for (int kt = 0; kt < n; ++kt) {
+            const bool win = kt >= lo && kt <= hi;
+            const bool glob = global_stride > 0 && kt % global_stride == 0;
+            if (win || glob) cols.push_back(kt);
+        }
+        rp[qt + 1] = int32_t(cols.size());
+    }
+    const int total = int(cols.size());
+    const int cap = *nnz;
+    *nnz = total;
+    if (cap < total || !kcols || !qrows) return ULYSSES_ERR_INVALID_ARG;
+    std::memcpy(rowptr, rp.data(), sizeof(int32_t) * (n + 1));
+    std::memcpy(kcols, cols.data(), sizeof(int32_t) * total);
+    // CSC by counting sort over key tiles; query tiles come out ascending
+    std::vector<int32_t> cnt(n + 1, 0);
+    for (int e = 0; e < total; ++e) cnt[cols[e] + 1]++;
+    for (int kt = 0; kt < n; ++kt) cnt[kt + 1] += cnt[kt];
+    std::memcpy(colptr, cnt.data(), sizeof(int32_t) * (n + 1));
+    std::vector<int32_t> pos(cnt.begin(), cnt.end() - 1);
+    for (int qt = 0; qt < n; ++qt)
+        for (int e = rp[qt]; e < rp[qt + 1]; ++e) qrows[pos[cols[e]]++] = qt;
+    return ULYSSES_OK;
+}
+
+int ulysses_get_device_status(void* stream, uint32_t* detail) {
+    uint32_t* err = device_error_word();
+    if (!err) return ULYSSES_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return ULYSSES_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_error_word_storage, sizeof(word)) != cudaSuccess) return ULYSSES_ERR_CUDA;
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word_storage, &zero, sizeof(zero)) != cudaSuccess) return ULYSSES_ERR_CUDA;
+    if (detail) *detail = word;
+    return word == 0 ? ULYSSES_OK : ULYSSES_ERR_DEVICE_TIMEOUT;
+}
+
+}  // extern "C"

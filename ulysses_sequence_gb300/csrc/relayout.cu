@@ -1,0 +1,153 @@
+// Standalone sequence<->head relayouts (the two all-to-alls of DeepSpeed-Ulysses, paper
+// summary section 3.4.1; pinyu.ai page "Use the other independent axis"), as on-device
+// permutations between the token-sharded [P][B][Lp][H][d] and head-sharded
+// [P][B][L][Hp][d] layouts.
+//
+// Both layouts keep one head group of one token contiguous: a "run" of Hp*d elements.
+// seq->head moves run (r, b, t, g) from in[((r*B + b)*Lp + t)*H*d + g*Hp*d] to
+// out[((g*B + b)*L + r*Lp + t)*Hp*d]; head->seq moves it back. Runs are at least 256 bytes
+// at every workload size, so 16-byte vector loads and stores are coalesced on both sides
+// without staging: a warp copies whole token rows, with index arithmetic once per row.
+#include "common.cuh"
+#include "ulysses_internal.h"
+
+namespace ulysses {
+
+struct RelayoutArgs {
+    const void* in;
+    void* out;
+    uint32_t P, B, Lp, L, H, d;
+    uint32_t rows;       // token rows P * B * Lp
+    uint32_t row_vecs;   // H * d / 8: 16-byte vectors of one token row (P runs)
+    uint32_t run_vecs;   // Hp * d / 8: 16-byte vectors of one run
+    int to_head;         // 1: seq->head, 0: head->seq
+};
+
+// A warp copies whole token rows (r, b, t): the token side of a row is contiguous, and
+// vector w of the row belongs to group g = w / run_vecs, which lands at
+// head[((g*B + b)*L + s)*run_vecs + w % run_vecs]. Each lane keeps the group offsets of
+// its VPL vectors in registers, so a row costs two integer divisions in total.
+template <int VPL, int UNROLL>
+__global__ void __launch_bounds__(256, 2) relayout_row_kernel(RelayoutArgs a) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+    const uint32_t gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint4* __restrict__ in = static_cast<const uint4*>(a.in);
+    uint4* __restrict__ out = static_cast<uint4*>(a.out);
+    // a tensor holds fewer than 2^32 vectors (checked by the launcher), so 32 bits suffice
+    const uint32_t group_stride = a.B * a.L * a.run_vecs;
+
+    uint32_t goff[VPL];
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+        const uint32_t w = lane + 32u * k;
+        const uint32_t g = w / a.run_vecs;
+        goff[k] = g * group_stride + (w - g * a.run_vecs);
+    }
+    const uint32_t BLp = a.B * a.Lp;
+
+    for (uint32_t row0 = gw * UNROLL; row0 < a.rows; row0 += nwarps * UNROLL) {
+        uint4 v[UNROLL][VPL];
+        uint64_t tok[UNROLL], head[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const uint32_t row = row0 + u;
+            const uint32_t rr = row < a.rows ? row : 0;
+            const uint32_t r = rr / BLp;
+            const uint32_t rem = rr - r * BLp;
+            const uint32_t b = rem / a.Lp;
+            const uint32_t t = rem - b * a.Lp;
+            tok[u] = uint64_t(rr) * a.row_vecs;
+            head[u] = (uint64_t(b) * a.L + uint64_t(r) * a.Lp + t) * a.run_vecs;
+            if (row < a.rows) {
+#pragma unroll
+                for (int k = 0; k < VPL; ++k) {
+                    const uint32_t w = lane + 32u * k;
+                    if (w < a.row_vecs) {
+                        const uint64_t src = a.to_head ? tok[u] + w : head[u] + goff[k];
+                        v[u][k] = __ldcs(in + src);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            if (row0 + u < a.rows) {
+#pragma unroll
+                for (int k = 0; k < VPL; ++k) {
+                    const uint32_t w = lane + 32u * k;
+                    if (w < a.row_vecs) {
+                        const uint64_t dst = a.to_head ? head[u] + goff[k] : tok[u] + w;
+                        __stcs(out + dst, v[u][k]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Fallback for shapes whose runs are not whole 16-byte vectors or buffers not 16-byte
+// aligned: one 2-byte element per thread.
+__global__ void relayout_elem_kernel(RelayoutArgs a, uint64_t total) {
+    const uint16_t* in = static_cast<const uint16_t*>(a.in);
+    uint16_t* out = static_cast<uint16_t*>(a.out);
+    const uint64_t run_elems = uint64_t(a.H / a.P) * a.d;
+    for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += uint64_t(gridDim.x) * blockDim.x) {
+        const uint64_t run = i / run_elems;
+        const uint64_t e = i - run * run_elems;
+        const uint64_t row = run / a.P;
+        const uint64_t g = run - row * a.P;
+        const uint64_t rb = row / a.Lp;
+        const uint64_t t = row - rb * a.Lp;
+        const uint64_t r = rb / a.B;
+        const uint64_t b = rb - r * a.B;
+        const uint64_t tok = i;
+        const uint64_t head = ((g * a.B + b) * a.L + r * a.Lp + t) * run_elems + e;
+        if (a.to_head) out[head] = in[tok];
+        else out[tok] = in[head];
+    }
+}
+
+int launch_relayout(const ulysses_shape_t& s, const void* in, void* out, cudaStream_t stream, bool to_head) {
+    RelayoutArgs a{};
+    a.in = in;
+    a.out = out;
+    a.P = s.P; a.B = s.B; a.L = s.L; a.Lp = s.L / s.P; a.H = s.H; a.d = s.d_h;
+    a.to_head = to_head ? 1 : 0;
+    const uint64_t rows = uint64_t(s.P) * s.B * a.Lp;
+    const uint64_t row_elems = uint64_t(s.H) * s.d_h;
+    const uint64_t run_elems = row_elems / s.P;
+    const uint64_t total = rows * row_elems;
+    if (total == 0) return ULYSSES_OK;
+    const int sms = device_sm_count();
+    constexpr int kThreads = 256;
+    const bool vec_ok = (run_elems % 8 == 0) && row_elems <= 8 * 512 && total / 8 < (1ull << 32) &&
+                        ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) % 16 == 0);
+    if (vec_ok) {
+        a.rows = static_cast<uint32_t>(rows);
+        a.row_vecs = static_cast<uint32_t>(row_elems / 8);
+        a.run_vecs = static_cast<uint32_t>(run_elems / 8);
+        const uint32_t vpl = (a.row_vecs + 31) / 32;
+        const int unroll = vpl <= 2 ? 8 : vpl <= 4 ? 4 : vpl <= 8 ? 2 : 1;
+        const uint64_t rows_per_cta = uint64_t(kThreads / 32) * unroll;
+        uint64_t blocks = (rows + rows_per_cta - 1) / rows_per_cta;
+        const uint64_t cap = uint64_t(sms) * 2;
+        if (blocks > cap) blocks = cap;
+        const unsigned nb = unsigned(blocks);
+        if (vpl <= 1) relayout_row_kernel<1, 8><<<nb, kThreads, 0, stream>>>(a);
+        else if (vpl <= 2) relayout_row_kernel<2, 8><<<nb, kThreads, 0, stream>>>(a);
+        else if (vpl <= 4) relayout_row_kernel<4, 4><<<nb, kThreads, 0, stream>>>(a);
+        else if (vpl <= 8) relayout_row_kernel<8, 2><<<nb, kThreads, 0, stream>>>(a);
+        else relayout_row_kernel<16, 1><<<nb, kThreads, 0, stream>>>(a);
+    } else {
+        RelayoutArgs e = a;
+        uint64_t blocks = (total + kThreads - 1) / kThreads;
+        const uint64_t cap = uint64_t(sms) * 16;
+        if (blocks > cap) blocks = cap;
+        relayout_elem_kernel<<<unsigned(blocks), kThreads, 0, stream>>>(e, total);
+    }
+    return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
+}
+
+}  // namespace ulysses

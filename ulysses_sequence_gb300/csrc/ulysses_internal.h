@@ -1,0 +1,47 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/ulysses.h"
+
+namespace ulysses {
+
+constexpr int kTile = 128;      // query / key tile edge of the attention kernels
+constexpr int kBwdQTile = 64;   // query rows per step of the backward kernel
+
+int device_sm_count();
+uint32_t* device_error_word();  // device address of this device's error word (nullptr on failure)
+
+// Encodes a 5-D bf16 tensor map over (d, head, row, batch, unit) with a box of
+// (64, 1, box_rows, 1, 1), 128-byte swizzle and zero fill out of bounds.
+//   token layout: dims (d, H, Lp, B, P);  head layout: dims (d, Hp, L, B, P).
+bool encode_qkv_map(CUtensorMap* map, const void* base, const ulysses_shape_t& s, int layout, int box_rows);
+
+struct MaskArgs {
+    int kind;
+    const int32_t* q_rowptr;
+    const int32_t* q_kcols;
+    const int32_t* k_colptr;
+    const int32_t* k_qrows;
+};
+
+int launch_relayout(const ulysses_shape_t& s, const void* in, void* out, cudaStream_t stream, bool to_head);
+
+int launch_attn_fwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, int layout, const void* q,
+                    const void* k, const void* v, void* o, float* lse, cudaStream_t stream);
+
+int launch_attn_bwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, int layout, const void* q,
+                    const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
+                    void* dk, void* dv, void* workspace, cudaStream_t stream);
+
+size_t bwd_workspace_bytes(const ulysses_shape_t& s);
+
+inline int gcd_int(int a, int b) {
+    while (b) { int t = a % b; a = b; b = t; }
+    return a;
+}
+
+}  // namespace ulysses
