@@ -156,18 +156,25 @@ def max_over_ranks(x: float, world: int) -> float:
 
 # ----------------------------------------------------------------------------- CPU oracle arm
 
-def oracle_sample_step(w: workloads.Workload, t_bits, rows, heads):
-    """One oracle pass (forward + backward) on a bounded sample of rows and heads.
-    Returns the algorithmic flops of the sample."""
+def sample_flops(w: workloads.Workload, rows, heads) -> int:
+    """Algorithmic flops of the oracle sample: permitted pairs of the sampled rows."""
     import oracle
     mask = oracle.mask_for(w)
     n_pairs = 0
-    for res in oracle.attention_sampled(t_bits["q"], t_bits["k"], t_bits["v"], t_bits["do"], w.P, mask, rows,
-                                        heads=heads):
-        allow = mask.rows(res["rows"], w.L)
-        n_pairs += int(allow.sum())
-    f = 4 * w.d * n_pairs + (8 * w.d * n_pairs if w.backward else 0)
-    return f
+    for b in range(w.B):
+        r = rows[rows[:, 0] == b, 1]
+        if len(r):
+            n_pairs += int(mask.rows(r, w.L).sum())
+    n_pairs *= len(heads)
+    return 4 * w.d * n_pairs + (8 * w.d * n_pairs if w.backward else 0)
+
+
+def oracle_sample_step(w: workloads.Workload, t_bits, rows, heads):
+    """One oracle pass (forward + backward) on a bounded sample of rows and heads."""
+    import oracle
+    for _ in oracle.attention_sampled(t_bits["q"], t_bits["k"], t_bits["v"], t_bits["do"], w.P, oracle.mask_for(w),
+                                      rows, heads=heads):
+        pass
 
 
 def cpu_sample(w: workloads.Workload, n_rows: int, n_heads: int):
@@ -183,14 +190,15 @@ def run_reference(args, w, world, rank):
     oracle.build()
     t = workloads.draw_workload(w)
     bits = {n: workloads.to_bf16_bits(x) for n, x in t.items()}
-    rows, heads = cpu_sample(w, args.cpu_rows, args.cpu_heads)
+    rows, heads = cpu_sample(w, args.ref_rows, args.ref_heads)
+    f_step = sample_flops(w, rows, heads)
     for _ in range(args.warmup):
         oracle_sample_step(w, bits, rows, heads)
     t0 = time.perf_counter()
-    f = 0
     for _ in range(args.steps):
-        f += oracle_sample_step(w, bits, rows, heads)
+        oracle_sample_step(w, bits, rows, heads)
     dt = time.perf_counter() - t0
+    f = f_step * args.steps
     value = f / dt / 1e12
     sample = f"{len(rows)} sampled query rows x {len(heads)} heads of {w.name}, fwd+bwd, per step"
     cores = os.cpu_count()
@@ -225,12 +233,18 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="gpt7b", choices=list(workloads.WORKLOADS))
-    ap.add_argument("--cpu-rows", type=int, default=64)
-    ap.add_argument("--cpu-heads", type=int, default=2)
+    ap.add_argument("--L", type=int, default=0, help="override the sequence length (smaller profiling cases)")
+    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--cpu-heads", type=int, default=4)
+    ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--ref-heads", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = workloads.WORKLOADS[args.workload]
+    if args.L:
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}@L{args.L}", L=args.L)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, w, world, rank)
@@ -345,8 +359,9 @@ def main():
             oracle.build()
             bits = {n: workloads.to_bf16_bits(v) for n, v in t.items()}
             rows, heads_s = cpu_sample(w, args.cpu_rows, args.cpu_heads)
+            fc = sample_flops(w, rows, heads_s)
             t0 = time.perf_counter()
-            fc = oracle_sample_step(w, bits, rows, heads_s)
+            oracle_sample_step(w, bits, rows, heads_s)
             dt = time.perf_counter() - t0
             cpu = {"value": fc / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                    "sample": f"{len(rows)} sampled query rows x {len(heads_s)} heads of {w.name}, fwd+bwd "

@@ -159,7 +159,7 @@ def mask_for(workload) -> Mask:
 # --------------------------------------------------------------------------- attention
 
 def _chunk_rows(L: int) -> int:
-    return max(1, min(4096, (1 << 24) // max(L, 1)))
+    return max(1, min(4096, (1 << 22) // max(L, 1)))
 
 
 def head_forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows: np.ndarray, mask: Mask,
@@ -264,14 +264,31 @@ def attention_full(q_tok: np.ndarray, k_tok: np.ndarray, v_tok: np.ndarray, P: i
     return out
 
 
+def _sampled_task(task):
+    """One (batch, head) of the sampled mode; runs in the caller or in a pool worker."""
+    b, h, rows, heads, mask, sc = task
+    conv = {nme: bf16_to_f64(x) if x.dtype == np.uint16 else x.astype(np.float64) for nme, x in heads.items()}
+    O, LSE = head_forward(conv["q"], conv["k"], conv["v"], rows, mask, sc)
+    res = {"b": b, "h": h, "rows": rows, "o": O, "lse": LSE}
+    if "do" in conv:
+        dQ, dK, dV = head_backward(conv["q"], conv["k"], conv["v"], conv["do"][rows], O, LSE, rows, mask, sc)
+        res.update(dq=dQ, dk=dK, dv=dV)
+    return res
+
+
+_BLAS_VARS = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+
+
 def attention_sampled(q_tok, k_tok, v_tok, do_tok, P: int, mask: Mask, rows_bi: np.ndarray,
-                      scale: Optional[float] = None, heads=None) -> Iterator[dict]:
+                      scale: Optional[float] = None, heads=None, workers: int = 0) -> Iterator[dict]:
     """Per-(batch, head) results on sampled query rows, for workloads too large to do whole.
 
     rows_bi: int [n, 2] of (b, i). For each (b, head) yields a dict with
       "b", "h", "rows" (sequence indices i), "o" [n_b, d], "lse" [n_b], and, when do_tok is
       given, "dq" [n_b, d] and "dk", "dv" [L, d]: the gradient contributions of the sampled
       rows (equal to the full dK, dV of a pass whose dO is zero on every other row).
+    (batch, head) pairs are independent; with workers > 1 they are spread over a process
+    pool started with "spawn" (results arrive in the same order).
     """
     head = {}
     for nme, t in (("q", q_tok), ("k", k_tok), ("v", v_tok), ("do", do_tok)):
@@ -280,18 +297,40 @@ def attention_sampled(q_tok, k_tok, v_tok, do_tok, P: int, mask: Mask, rows_bi: 
     _, B, L, Hp, d = head["q"].shape
     H = Hp * P
     sc = 1.0 / np.sqrt(d) if scale is None else scale
-    for b in range(B):
-        rows = rows_bi[rows_bi[:, 0] == b, 1]
-        if len(rows) == 0:
-            continue
-        for h in (range(H) if heads is None else heads):
-            g, j = divmod(h, Hp)
-            conv = {nme: bf16_to_f64(_head_view(y, g, b, j)) if y.dtype == np.uint16
-                    else _head_view(y, g, b, j).astype(np.float64) for nme, y in head.items()}
-            O, LSE = head_forward(conv["q"], conv["k"], conv["v"], rows, mask, sc)
-            res = {"b": b, "h": h, "rows": rows, "o": O, "lse": LSE}
-            if "do" in conv:
-                dQ, dK, dV = head_backward(conv["q"], conv["k"], conv["v"], conv["do"][rows], O, LSE,
-                                           rows, mask, sc)
-                res.update(dq=dQ, dk=dK, dv=dV)
-            yield res
+
+    def tasks():
+        for b in range(B):
+            rows = rows_bi[rows_bi[:, 0] == b, 1]
+            if len(rows) == 0:
+                continue
+            for h in (range(H) if heads is None else heads):
+                g, j = divmod(h, Hp)
+                yield (b, h, rows, {nme: np.ascontiguousarray(_head_view(y, g, b, j)) for nme, y in head.items()},
+                       mask, sc)
+
+    if workers <= 1:
+        for task in tasks():
+            yield _sampled_task(task)
+        return
+    import concurrent.futures
+    import multiprocessing
+    ctx = multiprocessing.get_context("spawn")
+    # one BLAS thread per worker (the pool supplies the parallelism): the variables must be
+    # in the environment when a worker starts, before it loads numpy
+    saved = {v: os.environ.get(v) for v in _BLAS_VARS}
+    os.environ.update({v: "1" for v in _BLAS_VARS})
+    try:
+        with concurrent.futures.ProcessPoolExecutor(max_workers=workers, mp_context=ctx) as ex:
+            pending = []
+            for task in tasks():
+                pending.append(ex.submit(_sampled_task, task))
+                if len(pending) >= 2 * workers:
+                    yield pending.pop(0).result()
+            for f in pending:
+                yield f.result()
+    finally:
+        for v, val in saved.items():
+            if val is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = val

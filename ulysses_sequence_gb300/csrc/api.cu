@@ -119,8 +119,8 @@ int validate_attn(const ulysses_shape_t& s, const ulysses_mask_t* mask, int layo
     }
     if (s.d_h != 64 && s.d_h != 128) return ULYSSES_ERR_UNSUPPORTED;
     if (layout == ULYSSES_LAYOUT_TOKEN_SHARDED && (s.L / s.P) % 8 != 0 && s.L > 0) return ULYSSES_ERR_UNSUPPORTED;
-    // grid limits: B*H CTAs along x, ceil(L / 128) along y
-    if (uint64_t(s.B) * s.H > 0x7fffffffull || (uint64_t(s.L) + kTile - 1) / kTile > 65535) return ULYSSES_ERR_UNSUPPORTED;
+    // grid limits: tiles along x, B*H along y
+    if (uint64_t(s.B) * s.H > 65535) return ULYSSES_ERR_UNSUPPORTED;
     return ULYSSES_OK;
 }
 

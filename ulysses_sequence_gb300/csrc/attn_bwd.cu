@@ -44,19 +44,20 @@ struct BwdParams {
 
 template <int D>
 struct BwdCfg {
+    static constexpr int NQ = 3;                            // query-step pipeline stages
     static constexpr uint32_t KT_BYTES = kTile * D * 2;     // 128-row key/value tile
     static constexpr uint32_t KCHUNK = kTile * 128;         // 128 rows x 64 elements
     static constexpr uint32_t QT_BYTES = kBwdQTile * D * 2; // 64-row query step
     static constexpr uint32_t QCHUNK = kBwdQTile * 128;     // 64 rows x 64 elements
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = OFF_K + KT_BYTES;
-    static constexpr uint32_t OFF_Q = OFF_V + KT_BYTES;          // [2]
-    static constexpr uint32_t OFF_DO = OFF_Q + 2 * QT_BYTES;     // [2]
-    static constexpr uint32_t OFF_PT = OFF_DO + 2 * QT_BYTES;    // 128 x 64 bf16
+    static constexpr uint32_t OFF_Q = OFF_V + KT_BYTES;           // [NQ]
+    static constexpr uint32_t OFF_DO = OFF_Q + NQ * QT_BYTES;     // [NQ]
+    static constexpr uint32_t OFF_PT = OFF_DO + NQ * QT_BYTES;    // 128 x 64 bf16
     static constexpr uint32_t OFF_DST = OFF_PT + kTile * kBwdQTile * 2;
-    static constexpr uint32_t OFF_LSE = OFF_DST + kTile * kBwdQTile * 2;  // [2][64] fp32
-    static constexpr uint32_t OFF_DELTA = OFF_LSE + 2 * kBwdQTile * 4;    // [2][64] fp32
-    static constexpr uint32_t OFF_BAR = OFF_DELTA + 2 * kBwdQTile * 4;
+    static constexpr uint32_t OFF_LSE = OFF_DST + kTile * kBwdQTile * 2;  // [NQ][64] fp32
+    static constexpr uint32_t OFF_DELTA = OFF_LSE + NQ * kBwdQTile * 4;   // [NQ][64] fp32
+    static constexpr uint32_t OFF_BAR = OFF_DELTA + NQ * kBwdQTile * 4;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     // TMEM columns
@@ -136,36 +137,39 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float* sLSE = reinterpret_cast<float*>(smem + C::OFF_LSE);
     float* sDelta = reinterpret_cast<float*>(smem + C::OFF_DELTA);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    constexpr int NQ = C::NQ;
     uint64_t* kv_full = bars + 0;
-    uint64_t* qdo_full = bars + 1;   // [2]
-    uint64_t* qdo_empty = bars + 3;  // [2]
-    uint64_t* s_full = bars + 5;
-    uint64_t* s_free = bars + 6;
-    uint64_t* dp_full = bars + 7;
-    uint64_t* dp_free = bars + 8;
-    uint64_t* p_full = bars + 9;
-    uint64_t* p_free = bars + 10;
-    uint64_t* ds_full = bars + 11;
-    uint64_t* ds_free = bars + 12;
-    uint64_t* dq_full = bars + 13;
-    uint64_t* dq_free = bars + 14;
-    uint64_t* dkdv_done = bars + 15;
-    uint64_t* drain = bars + 16;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+    uint64_t* qdo_full = bars + 1;          // [NQ]
+    uint64_t* qdo_empty = qdo_full + NQ;    // [NQ]
+    uint64_t* s_full = qdo_empty + NQ;
+    uint64_t* s_free = s_full + 1;
+    uint64_t* dp_full = s_full + 2;
+    uint64_t* dp_free = s_full + 3;
+    uint64_t* p_full = s_full + 4;
+    uint64_t* p_free = s_full + 5;
+    uint64_t* ds_full = s_full + 6;
+    uint64_t* ds_free = s_full + 7;
+    uint64_t* dq_full = s_full + 8;
+    uint64_t* dq_free = s_full + 9;
+    uint64_t* dkdv_done = s_full + 10;
+    uint64_t* drain = s_full + 11;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 12);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = static_cast<int>(warp_id());
     const int lane = static_cast<int>(lane_id());
-    const int bh = blockIdx.x;
+    // key tiles vary fastest, so the CTAs resident at one time share one head and its
+    // fp32 dQ accumulator stays in L2
+    const int bh = blockIdx.y;
     const int b = bh / p.H;
     const int h = bh % p.H;
-    const int kt = blockIdx.y;
+    const int kt = blockIdx.x;
     int q_first = 0;
     const int n_it = bwd_q_count<MASK>(p, kt, q_first);
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NQ; ++i) {
             mbar_init(qdo_full + i, 1);
             mbar_init(qdo_empty + i, 1);
         }
@@ -206,22 +210,33 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 bwd_load<D>(sK, &tm_k, kv_full, p, kt * kTile, kTile, p.box_rows_k, h, b);
                 bwd_load<D>(sV, &tm_v, kv_full, p, kt * kTile, kTile, p.box_rows_k, h, b);
             }
+            // lse and Delta arrive by bulk copy when the 64-row step is whole and 16-byte aligned
+            const bool bulk_stats = (p.L % 4) == 0;
             for (int it = 0; it < n_it; ++it) {
-                const int st = it & 1;
-                if (it >= 2) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(qdo_empty + st, ((it >> 1) - 1) & 1, ab, ROLE_LOAD, 1));
+                const int st = it % NQ;
+                if (it >= NQ) {
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(qdo_empty + st, ((it / NQ) - 1) & 1, ab, ROLE_LOAD, 1));
                     if (!ok) break;
                 }
                 const int q0 = bwd_q_step<MASK>(p, q_first, it) * kBwdQTile;
-                for (int c = lane; c < kBwdQTile; c += 32) {
-                    const int q = q0 + c;
-                    const bool in = q < p.L;
-                    sLSE[st * kBwdQTile + c] = in ? p.lse[stat_index(p, q, h, b)] * kLog2e : INFINITY;
-                    sDelta[st * kBwdQTile + c] = in ? p.delta[stat_index(p, q, h, b)] : 0.f;
+                const bool whole = bulk_stats && q0 + kBwdQTile <= p.L;
+                if (!whole) {
+                    for (int c = lane; c < kBwdQTile; c += 32) {
+                        const int q = q0 + c;
+                        const bool in = q < p.L;
+                        sLSE[st * kBwdQTile + c] = in ? p.lse[stat_index(p, q, h, b)] : INFINITY;
+                        sDelta[st * kBwdQTile + c] = in ? p.delta[stat_index(p, q, h, b)] : 0.f;
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(qdo_full + st, 2 * C::QT_BYTES);
+                    mbar_arrive_expect_tx(qdo_full + st, 2 * C::QT_BYTES + (whole ? 2 * kBwdQTile * 4 : 0));
+                    if (whole) {
+                        bulk_load(sLSE + st * kBwdQTile, p.lse + stat_index(p, q0, h, b), kBwdQTile * 4, qdo_full + st);
+                        bulk_load(sDelta + st * kBwdQTile, p.delta + stat_index(p, q0, h, b), kBwdQTile * 4,
+                                  qdo_full + st);
+                    }
                     bwd_load<D>(sQ + st * C::QT_BYTES, &tm_q, qdo_full + st, p, q0, kBwdQTile, p.box_rows_q, h, b);
                     bwd_load<D>(sDO + st * C::QT_BYTES, &tm_do, qdo_full + st, p, q0, kBwdQTile, p.box_rows_q, h, b);
                 }
@@ -229,8 +244,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             if (!ok && lane == 0) {
                 mbar_drain(kv_full, 0);
-                for (int st = 0; st < 2; ++st) {
-                    const int cnt = nq > st ? (nq - 1 - st) / 2 + 1 : 0;
+                for (int st = 0; st < NQ; ++st) {
+                    const int cnt = nq > st ? (nq - 1 - st) / NQ + 1 : 0;
                     if (cnt > 0) mbar_drain(qdo_full + st, (cnt - 1) & 1);
                 }
             }
@@ -245,12 +260,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint32_t aPt = smem_u32(sPt), aDSt = smem_u32(sDSt);
             const uint32_t tS = tmem + C::T_S, tDP = tmem + C::T_DP, tDQ = tmem + C::T_DQ;
             const uint32_t tDV = tmem + C::T_DV, tDK = tmem + C::T_DK;
-            // K^T as an MN-major A operand: the second 64-row block of M is the second d chunk;
-            // with d = 64 both halves read the same chunk and the upper lanes are ignored.
-            const uint32_t kt_lbo = (D == 128) ? C::KCHUNK : 0;
+            // K^T as an MN-major A operand: the second 64-row block of M is the second d chunk.
+            // With d = 64 that block reads the V tile behind K; those lanes of dQ^T are ignored.
+            const uint32_t kt_lbo = C::KCHUNK;
 
             auto issue_s_dp = [&](int j) {
-                const int st = j & 1;
+                const int st = j % NQ;
                 const uint32_t q = aQ + st * C::QT_BYTES, dO = aDO + st * C::QT_BYTES;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
@@ -274,7 +289,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 issue_s_dp(0);
             }
             for (int it = 0; ok && it < n_it; ++it) {
-                const int st = it & 1;
+                const int st = it % NQ;
                 const uint32_t q = aQ + st * C::QT_BYTES, dO = aDO + st * C::QT_BYTES;
                 // dV += P^T dO
                 if (!(ok = mbar_wait(p_full, it & 1, ab, ROLE_MMA, 3))) break;
@@ -286,7 +301,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 umma_commit(p_free);
                 // next step's S^T and dP^T overlap this step's dS computation
                 if (it + 1 < n_it) {
-                    if (!(ok = mbar_wait(qdo_full + ((it + 1) & 1), ((it + 1) >> 1) & 1, ab, ROLE_MMA, 4))) break;
+                    if (!(ok = mbar_wait(qdo_full + ((it + 1) % NQ), ((it + 1) / NQ) & 1, ab, ROLE_MMA, 4))) break;
                     if (!(ok = mbar_wait(s_free, it & 1, ab, ROLE_MMA, 5))) break;
                     if (!(ok = mbar_wait(dp_free, it & 1, ab, ROLE_MMA, 6))) break;
                     tc_fence_after();
@@ -323,9 +338,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t aPt = smem_u32(sPt), aDSt = smem_u32(sDSt);
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
-            const int st = it & 1;
+            const int st = it % NQ;
             const int q0 = bwd_q_step<MASK>(p, q_first, it) * kBwdQTile;
-            ok = __all_sync(0xffffffffu, mbar_wait(qdo_full + st, (it >> 1) & 1, ab, ROLE_SOFTMAX, 1) &&
+            ok = __all_sync(0xffffffffu, mbar_wait(qdo_full + st, (it / NQ) & 1, ab, ROLE_SOFTMAX, 1) &&
                                              mbar_wait(s_full, it & 1, ab, ROLE_SOFTMAX, 2));
             if (!ok) break;
             tc_fence_after();
@@ -336,11 +351,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);
-            const float* lse2 = sLSE + st * kBwdQTile;
+            const float* lse = sLSE + st * kBwdQTile;
             const bool diag = (MASK == ULYSSES_MASK_CAUSAL) && (q0 < kt * kTile + kTile);
 #pragma unroll
             for (int c = 0; c < kBwdQTile; ++c) {
-                float e = ex2(fmaf(pv[c], p.scale_log2, -lse2[c]));
+                float e = ex2(fmaf(pv[c], p.scale_log2, -lse[c] * kLog2e));
                 if (diag && q0 + c < key) e = 0.f;
                 pv[c] = e;
             }
@@ -436,7 +451,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int c = 0; c < kBwdQTile; ++c) {
                     const int q = q0 + c;
-                    if (q < p.L) atomicAdd(acc + size_t(q) * D + e, v[c]);
+                    if (q < p.L) red_add_f32(acc + size_t(q) * D + e, v[c]);
                 }
             }
         }
@@ -546,7 +561,7 @@ static int launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
             return ULYSSES_ERR_CUDA;
         attr_set[dev & 63] = true;
     }
-    dim3 grid(p.B * p.H, p.n_ktiles);
+    dim3 grid(p.n_ktiles, p.B * p.H);
     kern<<<grid, 320, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
     return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }

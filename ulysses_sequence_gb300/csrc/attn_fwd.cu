@@ -120,11 +120,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = static_cast<int>(warp_id());
     const int lane = static_cast<int>(lane_id());
-    const int bh = blockIdx.x;
+    // query tiles vary fastest (heaviest causal tiles first), so the CTAs resident at one
+    // time share one head and its K, V stay in L2
+    const int bh = blockIdx.y;
     const int b = bh / p.H;
     const int h = bh % p.H;
-    const int qt = (MASK == ULYSSES_MASK_CAUSAL) ? (p.n_tiles - 1 - static_cast<int>(blockIdx.y))
-                                                  : static_cast<int>(blockIdx.y);
+    const int qt = (MASK == ULYSSES_MASK_CAUSAL) ? (p.n_tiles - 1 - static_cast<int>(blockIdx.x))
+                                                  : static_cast<int>(blockIdx.x);
     int kv_first = 0;
     const int n_kv = fwd_kv_count<MASK>(p, qt, kv_first);
 
@@ -380,7 +382,7 @@ static int launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
             return ULYSSES_ERR_CUDA;
         attr_set[dev & 63] = true;
     }
-    dim3 grid(p.B * p.H, p.n_tiles);
+    dim3 grid(p.n_tiles, p.B * p.H);
     kern<<<grid, 192, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }
