@@ -14,7 +14,8 @@
 //        dP^T = V dO^T       (M=128, N=64, K=d)
 //        dV  += P^T dO       (M=128, N=d, K=64)     P^T bf16 written to shared memory
 //        dK  += dS^T Q       (M=128, N=d, K=64)     dS^T bf16 written to shared memory
-//        dQ^T = K^T dS^T     (M=d, N=64, K=128)     added into the fp32 accumulator
+//        dQ^T = K^T dS^T     (M=d, N=64, K=128)     added into the fp32 accumulator by
+//                                                   bulk reductions from shared memory
 //      Warps: 0 TMA producer (K, V once; Q, dO, lse, Delta per step, 2 stages), 1 MMA
 //      issuer, 2-5 thread-per-key softmax/dS, 6-9 thread-per-feature dQ reduction.
 //   3. bwd_dq_convert: dQ = bf16(scale * accumulator) into the output layout.
@@ -34,7 +35,7 @@ struct BwdParams {
     float scale_log2;
     const float* lse;    // [P][B][Hp][L]
     const float* delta;  // [P][B][Hp][L]
-    float* dq_acc;       // [B*H][L][D]
+    float* dq_acc;       // [B*H][n_qsteps][D/32][64][32]: one 8 KB block per (64 rows, 32 features)
     void* dk;
     void* dv;
     const int32_t* colptr;  // block-sparse CSC over key tiles
@@ -57,7 +58,9 @@ struct BwdCfg {
     static constexpr uint32_t OFF_DST = OFF_PT + kTile * kBwdQTile * 2;
     static constexpr uint32_t OFF_LSE = OFF_DST + kTile * kBwdQTile * 2;  // [NQ][64] fp32
     static constexpr uint32_t OFF_DELTA = OFF_LSE + NQ * kBwdQTile * 4;   // [NQ][64] fp32
-    static constexpr uint32_t OFF_BAR = OFF_DELTA + NQ * kBwdQTile * 4;
+    static constexpr uint32_t OFF_DQS = OFF_DELTA + NQ * kBwdQTile * 4;   // [4 warps][64][32] fp32
+    static constexpr uint32_t DQS_WARP_BYTES = kBwdQTile * 32 * 4;
+    static constexpr uint32_t OFF_BAR = OFF_DQS + 4 * DQS_WARP_BYTES;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     // TMEM columns
@@ -432,12 +435,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------------ dQ reduction
+        // Thread e holds dQ^T[e][0..63] of this step. Each warp stages its 32 features x 64
+        // rows in shared memory ([row][32] fp32, one 128-byte line per row) and adds the 8 KB
+        // block to the accumulator with one bulk reduction performed at L2.
         const int wq = warp & 3;
         const int e = wq * 32 + lane;  // feature index (TMEM lane of dQ^T)
         const uint32_t lane_off = uint32_t(wq * 32) << 16;
-        float* acc = p.dq_acc + size_t(b * p.H + h) * p.L * D;
+        const uint32_t stage = smem_u32(smem + C::OFF_DQS + wq * C::DQS_WARP_BYTES);
+        float* acc_head = p.dq_acc + size_t(b * p.H + h) * p.n_qsteps * kBwdQTile * D;
+        bool pending = false;
         for (int it = 0; it < n_it; ++it) {
-            const int q0 = bwd_q_step<MASK>(p, q_first, it) * kBwdQTile;
+            const int qs = bwd_q_step<MASK>(p, q_first, it);
             if (!__all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, ab, ROLE_DQ, 1))) break;
             tc_fence_after();
             float v[kBwdQTile];
@@ -447,14 +455,25 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dq_free);
-            if (e < D) {
-#pragma unroll
-                for (int c = 0; c < kBwdQTile; ++c) {
-                    const int q = q0 + c;
-                    if (q < p.L) red_add_f32(acc + size_t(q) * D + e, v[c]);
+            if (e < D) {  // warp-uniform: d = 64 leaves the upper two warps idle
+                if (pending) {
+                    if (lane == 0) bulk_wait_read_all();  // the previous block has left the stage
+                    __syncwarp();
                 }
+#pragma unroll
+                for (int c = 0; c < kBwdQTile; ++c) st_shared_f32(stage + c * 128 + lane * 4, v[c]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    float* dst = acc_head + (size_t(qs) * (D / 32) + wq) * (kBwdQTile * 32);
+                    bulk_reduce_add_f32(dst, smem + C::OFF_DQS + wq * C::DQS_WARP_BYTES, C::DQS_WARP_BYTES);
+                    bulk_commit();
+                }
+                pending = true;
             }
         }
+        if (pending && lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -504,14 +523,16 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p, const __nv_b
                     sum = fmaf(af.y, gf.y, sum);
                 }
             }
-            float4* acc = reinterpret_cast<float4*>(p.dq_acc + rr * D);
-#pragma unroll
-            for (int v = 0; v < D / 4 / LPR; ++v) acc[sub + v * LPR] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int m = LPR / 2; m > 0; m >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
         if (in && sub == 0) delta[stat_index(p, s, h, b)] = sum;
     }
+    // zero the fp32 dQ accumulator (tile layout, padded to whole 64-row steps)
+    const size_t n4 = size_t(p.B) * p.H * p.n_qsteps * kBwdQTile * D / 4;
+    float4* acc = reinterpret_cast<float4*>(p.dq_acc);
+    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += size_t(gridDim.x) * blockDim.x)
+        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // dQ = bf16(scale * accumulator), written in the output layout.
@@ -528,12 +549,14 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdParams p, __nv_b
         const int h = int(bh % p.H);
         const int b = int(bh / p.H);
         const size_t off = row_offset(p, s, h, b, D);
-        const float* acc = p.dq_acc + rr * D;
+        // tile layout [b*H + h][s / 64][e / 32][s % 64][e % 32]
+        const float* acc = p.dq_acc + (bh * p.n_qsteps + s / kBwdQTile) * size_t(kBwdQTile) * D + (s % kBwdQTile) * 32;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int e0 = (sub + v * LPR) * 8;
-            const float4 x0 = *reinterpret_cast<const float4*>(acc + e0);
-            const float4 x1 = *reinterpret_cast<const float4*>(acc + e0 + 4);
+            const float* a = acc + (e0 / 32) * (kBwdQTile * 32) + (e0 % 32);
+            const float4 x0 = *reinterpret_cast<const float4*>(a);
+            const float4 x1 = *reinterpret_cast<const float4*>(a + 4);
             *reinterpret_cast<uint4*>(dq + off + e0) =
                 make_uint4(pack_bf16(x0.x * p.scale, x0.y * p.scale), pack_bf16(x0.z * p.scale, x0.w * p.scale),
                            pack_bf16(x1.x * p.scale, x1.y * p.scale), pack_bf16(x1.z * p.scale, x1.w * p.scale));
@@ -541,11 +564,14 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdParams p, __nv_b
     }
 }
 
+static size_t acc_bytes(const ulysses_shape_t& s) {
+    const size_t steps = (size_t(s.L) + kBwdQTile - 1) / kBwdQTile;
+    return (size_t(s.B) * s.H * steps * kBwdQTile * s.d_h * 4 + 255) / 256 * 256;
+}
+
 size_t bwd_workspace_bytes(const ulysses_shape_t& s) {
     const size_t rows = size_t(s.B) * s.H * s.L;
-    const size_t acc = (rows * s.d_h * 4 + 255) / 256 * 256;
-    const size_t del = (rows * 4 + 255) / 256 * 256;
-    return acc + del;
+    return acc_bytes(s) + (rows * 4 + 255) / 256 * 256;
 }
 
 template <int D, int MASK>
@@ -603,9 +629,8 @@ int launch_attn_bwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, in
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.lse = lse;
-    const size_t rows = size_t(s.B) * s.H * s.L;
     p.dq_acc = static_cast<float*>(workspace);
-    p.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * s.d_h * 4 + 255) / 256 * 256);
+    p.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes(s));
     p.dk = dk;
     p.dv = dv;
     p.colptr = m.k_colptr;

@@ -5,7 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/ulysses.h"
+#include "ulysses.h"
 
 namespace ulysses {
 
