@@ -141,6 +141,29 @@ int ulysses_attn_bwd(ulysses_shape_t shape, const ulysses_mask_t *mask, float so
                      void *dq, void *dk, void *dv,
                      void *workspace, size_t workspace_bytes, void *stream);
 
+/* Size of the fixed device array behind ulysses_attn_bwd_noalloc (96 MiB). */
+#define ULYSSES_BWD_NOALLOC_SCRATCH_BYTES (96u * 1024u * 1024u)
+
+/* ulysses_attn_bwd without a workspace argument, for callers that cannot allocate device
+ * memory (for instance code whose device memory is owned entirely by a host framework's
+ * pool, or a runtime that may not call cudaMalloc after start-up). This entry point has no
+ * counterpart on the pages; it only changes where the workspace lives. It allocates
+ * nothing: the workspace is a file-scope device array of ULYSSES_BWD_NOALLOC_SCRATCH_BYTES
+ * that every GPU loading the library holds until the process exits.
+ *   - Arguments and results are those of ulysses_attn_bwd.
+ *   - Returns ULYSSES_ERR_UNSUPPORTED, launching nothing, when
+ *     ulysses_attn_bwd_workspace_size(shape) exceeds ULYSSES_BWD_NOALLOC_SCRATCH_BYTES
+ *     (for example B=1, L=8192, H=16, d_h=128 fits; B=1, L=32768, H=32, d_h=128 does not).
+ *   - The first call on a device looks up the array's device address with that device
+ *     current; make that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the contents of the last
+ *     call (the kernels re-zero what must start at zero). Calls whose work overlaps on the
+ *     GPU, from different streams or threads, race on it and give undefined results. */
+int ulysses_attn_bwd_noalloc(ulysses_shape_t shape, const ulysses_mask_t *mask, float softmax_scale,
+                             int io_layout, const void *q, const void *k, const void *v,
+                             const void *o, const float *lse, const void *dO,
+                             void *dq, void *dk, void *dv, void *stream);
+
 /* Host helper: the block-sparse pattern "sliding window plus strided global key tiles".
  * Query tile qt gets key tiles max(0, qt - window_before) .. min(n - 1, qt + window_after)
  * and every kt with kt % global_stride == 0 (global_stride <= 0: none), n = ceil(L/tile).

@@ -36,8 +36,9 @@ class MaskStruct(ctypes.Structure):
 
 
 EXPORTS = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_attn_fwd", "ulysses_attn_bwd_workspace_size",
-           "ulysses_attn_bwd", "ulysses_bsmask_build_window_global", "ulysses_get_device_status",
-           "ulysses_status_string")
+           "ulysses_attn_bwd", "ulysses_attn_bwd_noalloc", "ulysses_bsmask_build_window_global",
+           "ulysses_get_device_status", "ulysses_status_string")
+BWD_NOALLOC_SCRATCH_BYTES = 96 * 1024 * 1024  # ULYSSES_BWD_NOALLOC_SCRATCH_BYTES
 
 _lib = None
 
@@ -58,6 +59,8 @@ def load() -> ctypes.CDLL:
     lib.ulysses_attn_bwd_workspace_size.restype = sz
     lib.ulysses_attn_bwd.argtypes = [Shape, ctypes.POINTER(MaskStruct), f, i, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                      vp, sz, vp]
+    lib.ulysses_attn_bwd_noalloc.argtypes = [Shape, ctypes.POINTER(MaskStruct), f, i, vp, vp, vp, vp, vp, vp, vp, vp,
+                                             vp, vp]
     ip = ctypes.POINTER(ctypes.c_int32)
     lib.ulysses_bsmask_build_window_global.argtypes = [i, i, i, i, i, ip, ip, ip, ip, ctypes.POINTER(ctypes.c_int)]
     lib.ulysses_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -98,6 +101,14 @@ def ulysses_attn_bwd(shape: Shape, mask: MaskStruct, softmax_scale: float, io_la
                      stream: int) -> int:
     return load().ulysses_attn_bwd(shape, _mref(mask), softmax_scale, io_layout, q, k, v, o, lse, dO, dq, dk,
                                    dv, workspace, workspace_bytes, stream)
+
+
+def ulysses_attn_bwd_noalloc(shape: Shape, mask: MaskStruct, softmax_scale: float, io_layout: int, q: int, k: int,
+                             v: int, o: int, lse: int, dO: int, dq: int, dk: int, dv: int, stream: int) -> int:
+    """ulysses_attn_bwd with the workspace in the library's fixed device array (for callers
+    that cannot allocate device memory; see include/ulysses.h)."""
+    return load().ulysses_attn_bwd_noalloc(shape, _mref(mask), softmax_scale, io_layout, q, k, v, o, lse, dO, dq, dk,
+                                           dv, stream)
 
 
 def ulysses_bsmask_build_window_global(L: int, tile: int, window_before: int, window_after: int,
