@@ -12,11 +12,11 @@
 //      walking 64-row query steps. Per step, with S^T, dP^T in TMEM:
 //        S^T  = K Q^T        (M=128 keys, N=64 queries, K=d)
 //        dP^T = V dO^T       (M=128, N=64, K=d)
-//        dV  += P^T dO       (M=128, N=d, K=64)     P^T bf16 written to shared memory
+//        dV  += P^T dO       (M=128, N=d, K=64)     P^T bf16 in tensor memory (A operand)
 //        dK  += dS^T Q       (M=128, N=d, K=64)     dS^T bf16 written to shared memory
 //        dQ^T = K^T dS^T     (M=d, N=64, K=128)     added into the fp32 accumulator by
 //                                                   bulk reductions from shared memory
-//      Warps: 0 TMA producer (K, V once; Q, dO, lse, Delta per step, 2 stages), 1 MMA
+//      Warps: 0 TMA producer (K, V once; Q, dO, lse, Delta per step, 3 stages), 1 MMA
 //      issuer, 2-5 thread-per-key softmax/dS, 6-9 thread-per-feature dQ reduction.
 //   3. bwd_dq_convert: dQ = bf16(scale * accumulator) into the output layout.
 #include "common.cuh"
@@ -54,17 +54,17 @@ struct BwdCfg {
     static constexpr uint32_t OFF_V = OFF_K + KT_BYTES;
     static constexpr uint32_t OFF_Q = OFF_V + KT_BYTES;           // [NQ]
     static constexpr uint32_t OFF_DO = OFF_Q + NQ * QT_BYTES;     // [NQ]
-    static constexpr uint32_t OFF_PT = OFF_DO + NQ * QT_BYTES;    // 128 x 64 bf16
-    static constexpr uint32_t OFF_DST = OFF_PT + kTile * kBwdQTile * 2;
+    static constexpr uint32_t OFF_DST = OFF_DO + NQ * QT_BYTES;   // 128 x 64 bf16
     static constexpr uint32_t OFF_LSE = OFF_DST + kTile * kBwdQTile * 2;  // [NQ][64] fp32
     static constexpr uint32_t OFF_DELTA = OFF_LSE + NQ * kBwdQTile * 4;   // [NQ][64] fp32
-    static constexpr uint32_t OFF_DQS = OFF_DELTA + NQ * kBwdQTile * 4;   // [4 warps][64][32] fp32
-    static constexpr uint32_t DQS_WARP_BYTES = kBwdQTile * 32 * 4;
+    static constexpr int DQ_ROWS = 64;                                    // dQ rows staged per round
+    static constexpr uint32_t OFF_DQS = OFF_DELTA + NQ * kBwdQTile * 4;   // [4 warps][DQ_ROWS][32] fp32
+    static constexpr uint32_t DQS_WARP_BYTES = DQ_ROWS * 32 * 4;
     static constexpr uint32_t OFF_BAR = OFF_DQS + 4 * DQS_WARP_BYTES;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
-    // TMEM columns
-    static constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_DV = 256, T_DK = 384;
+    // TMEM columns (P^T: 64 bf16 per lane packed in 32 columns)
+    static constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_PT = 192, T_DV = 256, T_DK = 384;
 };
 
 __device__ __forceinline__ void bwd_coords(const BwdParams& p, int s, int h, int& c1, int& c2, int& c4) {
@@ -135,7 +135,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint8_t* sV = smem + C::OFF_V;
     uint8_t* sQ = smem + C::OFF_Q;
     uint8_t* sDO = smem + C::OFF_DO;
-    uint8_t* sPt = smem + C::OFF_PT;
     uint8_t* sDSt = smem + C::OFF_DST;
     float* sLSE = reinterpret_cast<float*>(smem + C::OFF_LSE);
     float* sDelta = reinterpret_cast<float*>(smem + C::OFF_DELTA);
@@ -260,7 +259,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             constexpr uint32_t id_kv = idesc_bf16(128, D, 0, 1);            // dV, dK
             constexpr uint32_t id_dq = idesc_bf16(128, kBwdQTile, 1, 1);    // dQ^T (M padded to 128 for d=64)
             const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO);
-            const uint32_t aPt = smem_u32(sPt), aDSt = smem_u32(sDSt);
+            const uint32_t aDSt = smem_u32(sDSt);
             const uint32_t tS = tmem + C::T_S, tDP = tmem + C::T_DP, tDQ = tmem + C::T_DQ;
             const uint32_t tDV = tmem + C::T_DV, tDK = tmem + C::T_DK;
             // K^T as an MN-major A operand: the second 64-row block of M is the second d chunk.
@@ -298,9 +297,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (!(ok = mbar_wait(p_full, it & 1, ab, ROLE_MMA, 3))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < kBwdQTile / 16; ++k)
-                    umma_ss(tDV, sdesc_sw128(aPt + k * 32, 16, 1024), sdesc_sw128(dO + k * 2048, C::QCHUNK, 1024),
-                            id_kv, (it > 0 || k > 0) ? 1u : 0u);
+                for (int k = 0; k < kBwdQTile / 16; ++k)  // 16 queries = 8 TMEM columns of P^T
+                    umma_ts(tDV, tmem + C::T_PT + k * 8, sdesc_sw128(dO + k * 2048, C::QCHUNK, 1024), id_kv,
+                            (it > 0 || k > 0) ? 1u : 0u);
                 umma_commit(p_free);
                 // next step's S^T and dP^T overlap this step's dS computation
                 if (it + 1 < n_it) {
@@ -338,7 +337,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int row = wq * 32 + lane;  // key row within the tile (TMEM lane)
         const uint32_t lane_off = uint32_t(wq * 32) << 16;
         const int key = kt * kTile + row;
-        const uint32_t aPt = smem_u32(sPt), aDSt = smem_u32(sDSt);
+        const uint32_t aDSt = smem_u32(sDSt);
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int st = it % NQ;
@@ -366,13 +365,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 ok = __all_sync(0xffffffffu, mbar_wait(p_free, (it - 1) & 1, ab, ROLE_SOFTMAX, 3));
                 if (!ok) break;
             }
+            {
+                uint32_t pk[32];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float* x = pv + u * 8;
-                st_shared_v4(aPt + sw128_offset(row, u), pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
-                             pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+                for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
+                tmem_st32_u(tmem + C::T_PT + lane_off, pk);
+                tmem_wait_st();
             }
-            fence_proxy_async_smem();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
 
@@ -437,7 +437,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // ------------------------------------------------------------------ dQ reduction
         // Thread e holds dQ^T[e][0..63] of this step. Each warp stages its 32 features x 64
         // rows in shared memory ([row][32] fp32, one 128-byte line per row) and adds the 8 KB
-        // block to the accumulator with one bulk reduction performed at L2.
+        // block to the accumulator with one bulk reduction performed at L2. (Staging in
+        // smaller rounds, to free room for a fourth query stage, measured slower.)
         const int wq = warp & 3;
         const int e = wq * 32 + lane;  // feature index (TMEM lane of dQ^T)
         const uint32_t lane_off = uint32_t(wq * 32) << 16;
@@ -456,20 +457,24 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(dq_free);
             if (e < D) {  // warp-uniform: d = 64 leaves the upper two warps idle
-                if (pending) {
-                    if (lane == 0) bulk_wait_read_all();  // the previous block has left the stage
-                    __syncwarp();
-                }
+                float* block = acc_head + (size_t(qs) * (D / 32) + wq) * (kBwdQTile * 32);
 #pragma unroll
-                for (int c = 0; c < kBwdQTile; ++c) st_shared_f32(stage + c * 128 + lane * 4, v[c]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    float* dst = acc_head + (size_t(qs) * (D / 32) + wq) * (kBwdQTile * 32);
-                    bulk_reduce_add_f32(dst, smem + C::OFF_DQS + wq * C::DQS_WARP_BYTES, C::DQS_WARP_BYTES);
-                    bulk_commit();
+                for (int r0 = 0; r0 < kBwdQTile; r0 += C::DQ_ROWS) {
+                    if (pending) {
+                        if (lane == 0) bulk_wait_read_all();  // the previous piece has left the stage
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int c = 0; c < C::DQ_ROWS; ++c) st_shared_f32(stage + c * 128 + lane * 4, v[r0 + c]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        bulk_reduce_add_f32(block + r0 * 32, smem + C::OFF_DQS + wq * C::DQS_WARP_BYTES,
+                                            C::DQS_WARP_BYTES);
+                        bulk_commit();
+                    }
+                    pending = true;
                 }
-                pending = true;
             }
         }
         if (pending && lane == 0) bulk_wait_all();

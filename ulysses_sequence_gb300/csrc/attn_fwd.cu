@@ -14,11 +14,14 @@
 //
 // Warp roles (192 threads):
 //   warp 0   TMA producer: Q once, then K and V tiles through an NS-stage ring;
-//   warp 1   MMA issuer: S = Q K^T into TMEM columns [0,128), O += P V into [128,128+d);
+//   warp 1   MMA issuer: S = Q K^T into TMEM columns [0,128); O += P V into [128,128+d)
+//            with P read from TMEM columns [256,320) (the A operand of a TMEM-sourced MMA);
 //   warps 2-5 softmax: thread i owns query row i (TMEM lane i): reads S from TMEM, masks,
-//            updates the running max and sum, writes P (bf16) to shared memory in the
-//            128-byte-swizzled K-major layout the MMA reads, rescales O in TMEM when the
-//            max grows by more than 2^8, and finally normalises and stores O and lse.
+//            updates the running max and sum, writes P as packed bf16 pairs into TMEM,
+//            rescales O in TMEM when the max grows by more than 2^8, and finally
+//            normalises and stores O and lse.
+// Keeping P in tensor memory leaves shared memory to the Q tile and three K/V stages, and
+// takes the P traffic off the shared-memory port that the MMA operand reads saturate.
 #include "common.cuh"
 #include "ulysses_internal.h"
 
@@ -39,17 +42,16 @@ struct FwdParams {
 
 template <int D>
 struct FwdCfg {
-    static constexpr int NS = (D == 64) ? 4 : 2;                 // K/V pipeline stages
+    static constexpr int NS = (D == 64) ? 6 : 3;                 // K/V pipeline stages
     static constexpr uint32_t TILE_BYTES = kTile * D * 2;       // one 128-row bf16 tile
     static constexpr uint32_t CHUNK_BYTES = kTile * 128;        // 128 rows x 64 elements
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + NS * TILE_BYTES;
-    static constexpr uint32_t OFF_P = OFF_V + NS * TILE_BYTES;
-    static constexpr uint32_t P_BYTES = kTile * kTile * 2;
-    static constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_V + NS * TILE_BYTES;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
-    static constexpr uint32_t TMEM_COLS = 256;
+    static constexpr uint32_t TMEM_COLS = 512;                    // S 128 | O 128 | P 64 (bf16 pairs)
+    static constexpr uint32_t T_S = 0, T_O = 128, T_P = 256;
 };
 
 // Coordinates of global row s of head h, batch b, in the 5-D map (d, head, row, batch, unit).
@@ -103,7 +105,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint8_t* sQ = smem + C::OFF_Q;
     uint8_t* sK = smem + C::OFF_K;
     uint8_t* sV = smem + C::OFF_V;
-    uint8_t* sP = smem + C::OFF_P;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* q_full = bars + 0;
     uint64_t* k_full = bars + 1;            // [NS]
@@ -151,8 +152,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem;
-    const uint32_t tO = tmem + 128;
+    const uint32_t tS = tmem + C::T_S;
+    const uint32_t tO = tmem + C::T_O;
+    const uint32_t tP = tmem + C::T_P;
     const Abort ab{abort_flag, p.err, KID_FWD};
 
     if (warp == 0) {
@@ -194,7 +196,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (lane == 0 && n_kv > 0) {
             constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t idO = idesc_bf16(128, D, 0, 1);
-            const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP);
+            const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
             bool ok = mbar_wait(q_full, 0, ab, ROLE_MMA, 1);
             for (int it = 0; ok && it <= n_kv; ++it) {
                 if (it < n_kv) {
@@ -220,12 +222,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tc_fence_after();
                     const uint32_t vbase = aV + st * C::TILE_BYTES;
 #pragma unroll
-                    for (int k = 0; k < kTile / 16; ++k) {
-                        const uint32_t poff = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
-                        umma_ss(tO, sdesc_sw128(aP + poff, 16, 1024),
-                                sdesc_sw128(vbase + k * 2048, C::CHUNK_BYTES, 1024), idO,
+                    for (int k = 0; k < kTile / 16; ++k)  // 16 keys = 8 TMEM columns of P per step
+                        umma_ts(tO, tP + k * 8, sdesc_sw128(vbase + k * 2048, C::CHUNK_BYTES, 1024), idO,
                                 (j > 0 || k > 0) ? 1u : 0u);
-                    }
                     umma_commit(pv_done);
                     umma_commit(v_empty + st);
                 }
@@ -244,7 +243,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         float m_used = -INFINITY;                 // running max, log2 domain
         float l_sum = 0.f;
         bool ok = true;
-        const uint32_t aP = smem_u32(sP);
         for (int it = 0; it < n_kv; ++it) {
             const int kt = fwd_kv_tile<MASK>(p, kv_first, it);
             ok = __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, ab, ROLE_SOFTMAX, 1));
@@ -303,15 +301,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             l_sum += rs;
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t pk[32];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float* x = s + ch * 64 + u * 8;
-                    st_shared_v4(aP + ch * C::CHUNK_BYTES + sw128_offset(row, u), pack_bf16(x[0], x[1]),
-                                 pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-                }
+                for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(s[h2 * 64 + 2 * i], s[h2 * 64 + 2 * i + 1]);
+                tmem_st32_u(tP + lane_off + h2 * 32, pk);
             }
-            fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);

@@ -192,6 +192,18 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]: the A operand (M rows = TMEM lanes, K along columns, two
+// bf16 per 32-bit column, lower K index in the low half) is read from tensor memory.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Makes the mbarrier track completion of every tcgen05 operation this thread issued so far.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -244,6 +256,11 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
           "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
           "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+
+// 32 lanes x 32 consecutive columns of raw 32-bit words (for packed bf16 pairs).
+__device__ __forceinline__ void tmem_st32_u(uint32_t taddr, const uint32_t* r) {
+    tmem_st32(taddr, reinterpret_cast<const float*>(r));
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
