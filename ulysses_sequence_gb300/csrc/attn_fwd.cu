@@ -1,5 +1,5 @@
 // Attention forward on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), one CTA per
-// (batch, head, 128-row query tile).
+// (batch, head, pair of 128-row query tiles).
 //
 // What it computes (paper summary section 3.4.1 "The challenge at the attention boundary";
 // pinyu.ai page "The layout that saves memory breaks at attention"): for one head over the
@@ -12,16 +12,22 @@
 // address computation (sender r = s / Lp, local token s % Lp). With the head-sharded
 // layout the same kernel reads [P][B][L][Hp][d].
 //
-// Warp roles (192 threads):
-//   warp 0   TMA producer: Q once, then K and V tiles through an NS-stage ring;
-//   warp 1   MMA issuer: S = Q K^T into TMEM columns [0,128); O += P V into [128,128+d)
-//            with P read from TMEM columns [256,320) (the A operand of a TMEM-sourced MMA);
-//   warps 2-5 softmax: thread i owns query row i (TMEM lane i): reads S from TMEM, masks,
-//            updates the running max and sum, writes P as packed bf16 pairs into TMEM,
-//            rescales O in TMEM when the max grows by more than 2^8, and finally
-//            normalises and stores O and lse.
-// Keeping P in tensor memory leaves shared memory to the Q tile and three K/V stages, and
-// takes the P traffic off the shared-memory port that the MMA operand reads saturate.
+// Two query tiles share every K/V tile brought into shared memory, which halves the K/V
+// traffic per flop; their softmax warpgroups alternate so that the tensor core works on
+// one tile while the other tile's softmax runs. Warp roles (320 threads):
+//   warp 0    TMA producer: both Q tiles once, then K and V tiles through their rings;
+//   warp 1    MMA issuer: S_t = Q_t K^T into TMEM columns [128 t, 128 t + 128) and
+//             O_t += P_t V into [256 + 128 t, ...), with P_t read from the first 64
+//             columns of S_t (packed bf16 pairs, the A operand of a TMEM-sourced MMA);
+//   warps 2-5 softmax of tile 0, warps 6-9 softmax of tile 1: thread i owns query row i
+//             (TMEM lane i): reads S_t in two 64-column halves for the row maximum, then
+//             again half by half to write P_t over S_t (keeping the live registers within
+//             the 168 a 10-warp CTA allows), rescales O_t in TMEM when the max grows by more
+//             than 2^8, and finally normalises and stores O_t and lse.
+// The MMA issuer issues PV_t for a key tile before S_t for the next one, and tcgen05
+// operations of one thread complete in order: when S_t of a key tile is complete, the
+// previous PV_t (which read P_t from the same columns) is too, so O_t may be rescaled and
+// the columns reused without a further wait.
 #include "common.cuh"
 #include "ulysses_internal.h"
 
@@ -31,6 +37,7 @@ struct FwdParams {
     int B, L, H, Hp, Lp, P;
     int layout;      // 0 token-sharded, 1 head-sharded
     int n_tiles;     // ceil(L / 128)
+    int n_pairs;     // ceil(n_tiles / 2)
     int box_rows;    // rows per TMA box (divides 128; boxes never straddle a shard)
     float scale_log2;
     void* o;
@@ -42,16 +49,17 @@ struct FwdParams {
 
 template <int D>
 struct FwdCfg {
-    static constexpr int NS = (D == 64) ? 6 : 3;                 // K/V pipeline stages
+    static constexpr int NSK = (D == 64) ? 6 : 3;                // K pipeline stages
+    static constexpr int NSV = (D == 64) ? 6 : 2;                // V pipeline stages
     static constexpr uint32_t TILE_BYTES = kTile * D * 2;       // one 128-row bf16 tile
     static constexpr uint32_t CHUNK_BYTES = kTile * 128;        // 128 rows x 64 elements
-    static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
-    static constexpr uint32_t OFF_V = OFF_K + NS * TILE_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_V + NS * TILE_BYTES;
-    static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
-    static constexpr uint32_t TMEM_COLS = 512;                    // S 128 | O 128 | P 64 (bf16 pairs)
-    static constexpr uint32_t T_S = 0, T_O = 128, T_P = 256;
+    static constexpr uint32_t OFF_Q = 0;                        // [2] query tiles
+    static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
+    static constexpr uint32_t OFF_V = OFF_K + NSK * TILE_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_V + NSV * TILE_BYTES;
+    static constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;  // + barriers + alignment slack
+    static constexpr uint32_t TMEM_COLS = 512;                    // S0 | S1 | O0 | O1
+    static constexpr uint32_t kThreads = 320;
 };
 
 // Coordinates of global row s of head h, batch b, in the 5-D map (d, head, row, batch, unit).
@@ -80,26 +88,57 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, 
     }
 }
 
+// Key tiles of one query tile, in ascending order.
 template <int MASK>
-__device__ __forceinline__ int fwd_kv_count(const FwdParams& p, int qt, int& first) {
-    if (MASK == ULYSSES_MASK_CAUSAL) { first = 0; return qt + 1; }
-    if (MASK == ULYSSES_MASK_NONE) { first = 0; return p.n_tiles; }
-    first = p.rowptr[qt];
-    return p.rowptr[qt + 1] - first;
-}
+struct TileList {
+    int n, first;
+    const int32_t* cols;
+    __device__ __forceinline__ void init(const FwdParams& p, int qt, bool exists) {
+        cols = p.kcols;
+        first = 0;
+        if (!exists) n = 0;
+        else if (MASK == ULYSSES_MASK_CAUSAL) n = qt + 1;
+        else if (MASK == ULYSSES_MASK_NONE) n = p.n_tiles;
+        else { first = p.rowptr[qt]; n = p.rowptr[qt + 1] - first; }
+    }
+    __device__ __forceinline__ int kt(int c) const {
+        return MASK == ULYSSES_MASK_BLOCK_SPARSE ? cols[first + c] : c;
+    }
+};
 
+// The merged, ascending key-tile sequence of the CTA's two query tiles: each step names a
+// key tile and which of the two tiles use it.
 template <int MASK>
-__device__ __forceinline__ int fwd_kv_tile(const FwdParams& p, int first, int it) {
-    if (MASK == ULYSSES_MASK_BLOCK_SPARSE) return p.kcols[first + it];
-    return it;
-}
+struct PairSeq {
+    TileList<MASK> t0, t1;
+    int c0, c1;
+    __device__ __forceinline__ void init(const FwdParams& p, int qt0, bool has1) {
+        t0.init(p, qt0, true);
+        t1.init(p, qt0 + 1, has1);
+        c0 = c1 = 0;
+    }
+    // returns false when both lists are exhausted
+    __device__ __forceinline__ bool next(int& kt, bool& in0, bool& in1) {
+        const bool a0 = c0 < t0.n, a1 = c1 < t1.n;
+        if (!a0 && !a1) return false;
+        const int k0 = a0 ? t0.kt(c0) : 0x7fffffff;
+        const int k1 = a1 ? t1.kt(c1) : 0x7fffffff;
+        kt = k0 < k1 ? k0 : k1;
+        in0 = a0 && k0 == kt;
+        in1 = a1 && k1 == kt;
+        c0 += in0;
+        c1 += in1;
+        return true;
+    }
+};
 
 template <int D, int MASK>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
     using C = FwdCfg<D>;
-    constexpr int NS = C::NS;
+    constexpr int NSK = C::NSK;
+    constexpr int NSV = C::NSV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem + C::OFF_Q;
@@ -107,42 +146,44 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint8_t* sV = smem + C::OFF_V;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* q_full = bars + 0;
-    uint64_t* k_full = bars + 1;            // [NS]
-    uint64_t* k_empty = k_full + NS;        // [NS]
-    uint64_t* v_full = k_empty + NS;        // [NS]
-    uint64_t* v_empty = v_full + NS;        // [NS]
-    uint64_t* s_full = v_empty + NS;
-    uint64_t* s_free = s_full + 1;
-    uint64_t* p_full = s_free + 1;
-    uint64_t* pv_done = p_full + 1;
-    uint64_t* drain = pv_done + 1;
+    uint64_t* k_full = bars + 1;            // [NSK]
+    uint64_t* k_empty = k_full + NSK;       // [NSK]
+    uint64_t* v_full = k_empty + NSK;       // [NSV]
+    uint64_t* v_empty = v_full + NSV;       // [NSV]
+    uint64_t* s_full = v_empty + NSV;       // [2]
+    uint64_t* p_full = s_full + 2;          // [2]
+    uint64_t* o_done = p_full + 2;
+    uint64_t* drain = o_done + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = static_cast<int>(warp_id());
     const int lane = static_cast<int>(lane_id());
-    // query tiles vary fastest (heaviest causal tiles first), so the CTAs resident at one
-    // time share one head and its K, V stay in L2
+    // query-tile pairs vary fastest (heaviest causal pairs first), so the CTAs resident at
+    // one time share one head and its K, V stay in L2
     const int bh = blockIdx.y;
     const int b = bh / p.H;
     const int h = bh % p.H;
-    const int qt = (MASK == ULYSSES_MASK_CAUSAL) ? (p.n_tiles - 1 - static_cast<int>(blockIdx.x))
-                                                  : static_cast<int>(blockIdx.x);
-    int kv_first = 0;
-    const int n_kv = fwd_kv_count<MASK>(p, qt, kv_first);
+    const int pair = (MASK == ULYSSES_MASK_CAUSAL) ? (p.n_pairs - 1 - static_cast<int>(blockIdx.x))
+                                                    : static_cast<int>(blockIdx.x);
+    const int qt0 = 2 * pair;
+    const bool has1 = qt0 + 1 < p.n_tiles;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < NS; ++i) {
+        for (int i = 0; i < NSK; ++i) {
             mbar_init(k_full + i, 1);
             mbar_init(k_empty + i, 1);
+        }
+        for (int i = 0; i < NSV; ++i) {
             mbar_init(v_full + i, 1);
             mbar_init(v_empty + i, 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(s_free, 4);
-        mbar_init(p_full, 4);
-        mbar_init(pv_done, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(s_full + t, 1);
+            mbar_init(p_full + t, 4);
+        }
+        mbar_init(o_done, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -152,169 +193,222 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem + C::T_S;
-    const uint32_t tO = tmem + C::T_O;
-    const uint32_t tP = tmem + C::T_P;
     const Abort ab{abort_flag, p.err, KID_FWD};
-
-    if (warp == 0) {
+    if (warp < 2) {
+      if (warp == 0) {
         // ------------------------------------------------------------------ producer
-        if (lane == 0 && n_kv > 0) {
+        if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
+            PairSeq<MASK> seq;
+            seq.init(p, qt0, has1);
             int nk = 0, nv = 0;  // loads issued so far, per tensor
             bool ok = true;
-            mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
-            load_tile<D>(sQ, &tm_q, q_full, p, qt * kTile, h, b);
-            for (int it = 0; it < n_kv; ++it) {
-                const int st = it % NS;
-                const uint32_t ph = (it / NS) & 1;
-                const int kt = fwd_kv_tile<MASK>(p, kv_first, it);
-                if (it >= NS && !(ok = mbar_wait(k_empty + st, ph ^ 1, ab, ROLE_LOAD, 1))) break;
-                mbar_arrive_expect_tx(k_full + st, C::TILE_BYTES);
-                load_tile<D>(sK + st * C::TILE_BYTES, &tm_k, k_full + st, p, kt * kTile, h, b);
+            bool any = false;
+            int kt;
+            bool in0, in1;
+            for (int j = 0; seq.next(kt, in0, in1); ++j) {
+                if (!any) {
+                    any = true;
+                    mbar_arrive_expect_tx(q_full, 2 * C::TILE_BYTES);
+                    load_tile<D>(sQ, &tm_q, q_full, p, qt0 * kTile, h, b);
+                    load_tile<D>(sQ + C::TILE_BYTES, &tm_q, q_full, p, (qt0 + 1) * kTile, h, b);
+                }
+                const int sk = j % NSK, sv = j % NSV;
+                if (j >= NSK && !(ok = mbar_wait(k_empty + sk, ((j / NSK) - 1) & 1, ab, ROLE_LOAD, 1))) break;
+                mbar_arrive_expect_tx(k_full + sk, C::TILE_BYTES);
+                load_tile<D>(sK + sk * C::TILE_BYTES, &tm_k, k_full + sk, p, kt * kTile, h, b);
                 ++nk;
-                if (it >= NS && !(ok = mbar_wait(v_empty + st, ph ^ 1, ab, ROLE_LOAD, 2))) break;
-                mbar_arrive_expect_tx(v_full + st, C::TILE_BYTES);
-                load_tile<D>(sV + st * C::TILE_BYTES, &tm_v, v_full + st, p, kt * kTile, h, b);
+                if (j >= NSV && !(ok = mbar_wait(v_empty + sv, ((j / NSV) - 1) & 1, ab, ROLE_LOAD, 2))) break;
+                mbar_arrive_expect_tx(v_full + sv, C::TILE_BYTES);
+                load_tile<D>(sV + sv * C::TILE_BYTES, &tm_v, v_full + sv, p, kt * kTile, h, b);
                 ++nv;
             }
             if (!ok) {
                 // let copies already in flight land before the CTA can exit
                 mbar_drain(q_full, 0);
-                for (int st = 0; st < NS; ++st) {
-                    const int ck = nk > st ? (nk - 1 - st) / NS + 1 : 0;  // K loads issued to stage st
-                    const int cv = nv > st ? (nv - 1 - st) / NS + 1 : 0;
+                for (int st = 0; st < NSK; ++st) {
+                    const int ck = nk > st ? (nk - 1 - st) / NSK + 1 : 0;  // K loads issued to stage st
                     if (ck > 0) mbar_drain(k_full + st, (ck - 1) & 1);
+                }
+                for (int st = 0; st < NSV; ++st) {
+                    const int cv = nv > st ? (nv - 1 - st) / NSV + 1 : 0;
                     if (cv > 0) mbar_drain(v_full + st, (cv - 1) & 1);
                 }
             }
         }
-    } else if (warp == 1) {
+      } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_kv > 0) {
+        if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t idO = idesc_bf16(128, D, 0, 1);
             const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-            bool ok = mbar_wait(q_full, 0, ab, ROLE_MMA, 1);
-            for (int it = 0; ok && it <= n_kv; ++it) {
-                if (it < n_kv) {
-                    const int st = it % NS;
-                    if (!(ok = mbar_wait(k_full + st, (it / NS) & 1, ab, ROLE_MMA, 2))) break;
-                    if (it > 0 && !(ok = mbar_wait(s_free, (it - 1) & 1, ab, ROLE_MMA, 3))) break;
-                    tc_fence_after();
-                    const uint32_t kbase = aK + st * C::TILE_BYTES;
+            PairSeq<MASK> seq;
+            seq.init(p, qt0, has1);
+            int kt, nkt;
+            bool in0, in1, nin0 = false, nin1 = false;
+            bool ok = true;
+            bool cur = seq.next(kt, in0, in1);
+            // S_t = Q_t K^T for the key tile in K stage sk
+            auto issue_s = [&](int t, int sk) {
+                const uint32_t q = aQ + t * C::TILE_BYTES, kb = aK + sk * C::TILE_BYTES;
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
-                        umma_ss(tS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), idS,
-                                k > 0 ? 1u : 0u);
-                    }
-                    umma_commit(s_full);
-                    umma_commit(k_empty + st);
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
+                    umma_ss(tmem + 128 * t, sdesc_sw128(q + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idS,
+                            k > 0 ? 1u : 0u);
                 }
-                if (it > 0) {
-                    const int j = it - 1;
-                    const int st = j % NS;
-                    if (!(ok = mbar_wait(p_full, j & 1, ab, ROLE_MMA, 4))) break;
-                    if (!(ok = mbar_wait(v_full + st, (j / NS) & 1, ab, ROLE_MMA, 5))) break;
-                    tc_fence_after();
-                    const uint32_t vbase = aV + st * C::TILE_BYTES;
+                umma_commit(s_full + t);
+            };
+            // O_t += P_t V for the value tile in V stage sv
+            auto issue_pv = [&](int t, int sv, bool first) {
+                const uint32_t vb = aV + sv * C::TILE_BYTES;
 #pragma unroll
-                    for (int k = 0; k < kTile / 16; ++k)  // 16 keys = 8 TMEM columns of P per step
-                        umma_ts(tO, tP + k * 8, sdesc_sw128(vbase + k * 2048, C::CHUNK_BYTES, 1024), idO,
-                                (j > 0 || k > 0) ? 1u : 0u);
-                    umma_commit(pv_done);
-                    umma_commit(v_empty + st);
+                for (int k = 0; k < kTile / 16; ++k)  // 16 keys = 8 TMEM columns of P per step
+                    umma_ts(tmem + 256 + 128 * t, tmem + 128 * t + k * 8,
+                            sdesc_sw128(vb + k * 2048, C::CHUNK_BYTES, 1024), idO, (!first || k > 0) ? 1u : 0u);
+            };
+            if (cur) {
+                ok = mbar_wait(q_full, 0, ab, ROLE_MMA, 1) && mbar_wait(k_full, 0, ab, ROLE_MMA, 2);
+                if (ok) {
+                    tc_fence_after();
+                    if (in0) issue_s(0, 0);
+                    if (in1) issue_s(1, 0);
+                    umma_commit(k_empty);
                 }
             }
-            if (!ok) {
+            int c0 = 0, c1 = 0;  // PV MMAs issued per tile
+            for (int j = 0; ok && cur; ++j) {
+                const bool nxt = seq.next(nkt, nin0, nin1);
+                const int sv = j % NSV, skn = (j + 1) % NSK;
+                if (!(ok = mbar_wait(v_full + sv, (j / NSV) & 1, ab, ROLE_MMA, 3))) break;
+                if (in0) {
+                    if (!(ok = mbar_wait(p_full, c0 & 1, ab, ROLE_MMA, 4))) break;
+                    tc_fence_after();
+                    issue_pv(0, sv, c0 == 0);
+                    ++c0;
+                }
+                if (nxt) {
+                    if (!(ok = mbar_wait(k_full + skn, ((j + 1) / NSK) & 1, ab, ROLE_MMA, 5))) break;
+                    tc_fence_after();
+                    if (nin0) issue_s(0, skn);
+                }
+                if (in1) {
+                    if (!(ok = mbar_wait(p_full + 1, c1 & 1, ab, ROLE_MMA, 6))) break;
+                    tc_fence_after();
+                    issue_pv(1, sv, c1 == 0);
+                    ++c1;
+                }
+                if (nxt) {
+                    if (nin1) issue_s(1, skn);
+                    umma_commit(k_empty + skn);
+                }
+                umma_commit(v_empty + sv);
+                cur = nxt;
+                kt = nkt;
+                in0 = nin0;
+                in1 = nin1;
+            }
+            if (ok) umma_commit(o_done);
+            else {
                 umma_commit(drain);
                 mbar_drain(drain, 0);
             }
         }
+      }
     } else {
-        // ------------------------------------------------------------------ softmax
+        // ------------------------------------------------------------------ softmax (tile t)
+        const int t = warp < 6 ? 0 : 1;
         const int wq = warp & 3;                  // TMEM lane quadrant of this warp
         const int row = wq * 32 + lane;           // query row within the tile (TMEM lane)
         const uint32_t lane_off = uint32_t(wq * 32) << 16;
+        const int qt = qt0 + t;
         const int s_row = qt * kTile + row;       // global query index
+        const uint32_t tS = tmem + 128 * t;
+        const uint32_t tO = tmem + 256 + 128 * t;
+        TileList<MASK> list;
+        list.init(p, qt, t == 0 || has1);
         float m_used = -INFINITY;                 // running max, log2 domain
         float l_sum = 0.f;
         bool ok = true;
-        for (int it = 0; it < n_kv; ++it) {
-            const int kt = fwd_kv_tile<MASK>(p, kv_first, it);
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, ab, ROLE_SOFTMAX, 1));
+        for (int c = 0; c < list.n; ++c) {
+            const int kt = list.kt(c);
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full + t, c & 1, ab, ROLE_SOFTMAX, 1));
             if (!ok) break;
             tc_fence_after();
-            float s[kTile];
-#pragma unroll
-            for (int c = 0; c < kTile / 32; ++c) tmem_ld32(tS + lane_off + c * 32, s + c * 32);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);
-
             const int k0 = kt * kTile;
             const bool diag = (MASK == ULYSSES_MASK_CAUSAL) && (kt == qt);
-            const bool tail = k0 + kTile > p.L;
-            if (diag || tail) {
+            const bool masked = diag || (k0 + kTile > p.L);
+            // keys past the diagonal (causal) or past the end of the sequence are excluded
+            auto mask_half = [&](float* v, int c0) {
+                if (masked) {
 #pragma unroll
-                for (int c = 0; c < kTile; ++c) {
-                    const int key = k0 + c;
-                    if ((diag && key > s_row) || key >= p.L) s[c] = -INFINITY;
+                    for (int i = 0; i < 64; ++i) {
+                        const int key = k0 + c0 + i;
+                        if ((diag && key > s_row) || key >= p.L) v[i] = -INFINITY;
+                    }
                 }
-            }
+            };
+            // pass 1: row maximum
             float mx = -INFINITY;
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                float v[64];
+                tmem_ld32(tS + lane_off + hh * 64, v);
+                tmem_ld32(tS + lane_off + hh * 64 + 32, v + 32);
+                tmem_wait_ld();
+                mask_half(v, hh * 64);
 #pragma unroll
-            for (int c = 0; c < kTile; ++c) mx = fmaxf(mx, s[c]);
+                for (int i = 0; i < 64; ++i) mx = fmaxf(mx, v[i]);
+            }
             const float m_new = fmaxf(m_used, mx * p.scale_log2);
             const bool need = m_new > m_used + 8.0f;
-            if (it > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (it - 1) & 1, ab, ROLE_SOFTMAX, 2));
-                if (!ok) break;
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, need)) {
-                    const float alpha = need ? ex2(m_used - m_new) : 1.0f;
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(tO + lane_off + c * 32, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tmem_st32(tO + lane_off + c * 32, o);
-                    }
-                    tmem_wait_st();
-                    l_sum *= alpha;
-                }
-            }
+            const float alpha = need ? ex2(m_used - m_new) : 1.0f;  // ex2(-inf) = 0 for a first max
             if (need) m_used = m_new;
             const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+            // pass 2: P = 2^(S*scale*log2e - m) as bf16 pairs over the first 64 columns of S_t
+            // (half hh of S lands in columns [32 hh, 32 hh + 32), already read)
             float rs = 0.f;
-#pragma unroll
-            for (int c = 0; c < kTile; ++c) {
-                const float e = ex2(fmaf(s[c], p.scale_log2, neg_m));
-                s[c] = e;
-                rs += e;
-            }
-            l_sum += rs;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                float v[64];
+                tmem_ld32(tS + lane_off + hh * 64, v);
+                tmem_ld32(tS + lane_off + hh * 64 + 32, v + 32);
+                tmem_wait_ld();
+                mask_half(v, hh * 64);
                 uint32_t pk[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(s[h2 * 64 + 2 * i], s[h2 * 64 + 2 * i + 1]);
-                tmem_st32_u(tP + lane_off + h2 * 32, pk);
+                for (int i = 0; i < 32; ++i) {
+                    const float e0 = ex2(fmaf(v[2 * i], p.scale_log2, neg_m));
+                    const float e1 = ex2(fmaf(v[2 * i + 1], p.scale_log2, neg_m));
+                    rs += e0 + e1;
+                    pk[i] = pack_bf16(e0, e1);
+                }
+                tmem_st32_u(tS + lane_off + hh * 32, pk);
+            }
+            l_sum = l_sum * alpha + rs;
+            // O_t is stable (the previous PV_t was issued before this S_t and has completed);
+            // rescale it before this step's PV_t, which waits for the arrival below
+            if (c > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+                for (int i = 0; i < D / 32; ++i) {
+                    float o[32];
+                    tmem_ld32(tO + lane_off + i * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) o[x] *= alpha;
+                    tmem_st32(tO + lane_off + i * 32, o);
+                }
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(p_full + t);
         }
 
         // ------------------------------------------------------------------ epilogue
-        if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (n_kv - 1) & 1, ab, ROLE_EPI, 1));
+        if (ok && list.n > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done, 0, ab, ROLE_EPI, 1));
         if (ok) {
             tc_fence_after();
             const bool valid = s_row < p.L;
@@ -322,8 +416,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const float inv_l = any_key ? 1.0f / l_sum : 0.f;
             __nv_bfloat16* orow;
             if (p.layout == ULYSSES_LAYOUT_TOKEN_SHARDED) {
-                const int r = s_row / p.Lp, t = s_row % p.Lp;
-                orow = static_cast<__nv_bfloat16*>(p.o) + ((size_t(r) * p.B + b) * p.Lp + t) * size_t(p.H) * D +
+                const int r = s_row / p.Lp, tt = s_row % p.Lp;
+                orow = static_cast<__nv_bfloat16*>(p.o) + ((size_t(r) * p.B + b) * p.Lp + tt) * size_t(p.H) * D +
                        size_t(h) * D;
             } else {
                 const int g = h / p.Hp, j = h % p.Hp;
@@ -331,16 +425,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                        size_t(j) * D;
             }
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int i = 0; i < D / 32; ++i) {
                 float o[32];
-                if (n_kv > 0) {
-                    tmem_ld32(tO + lane_off + c * 32, o);
+                if (list.n > 0) {
+                    tmem_ld32(tO + lane_off + i * 32, o);
                     tmem_wait_ld();
                 }
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = (n_kv > 0) ? o[i] * inv_l : 0.f;
+                for (int x = 0; x < 32; ++x) o[x] = (list.n > 0) ? o[x] * inv_l : 0.f;
                 if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+                    uint4* dst = reinterpret_cast<uint4*>(orow + i * 32);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         dst[v] = make_uint4(pack_bf16(o[8 * v + 0], o[8 * v + 1]), pack_bf16(o[8 * v + 2], o[8 * v + 3]),
@@ -378,8 +472,8 @@ static int launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
             return ULYSSES_ERR_CUDA;
         attr_set[dev & 63] = true;
     }
-    dim3 grid(p.n_tiles, p.B * p.H);
-    kern<<<grid, 192, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+    dim3 grid(p.n_pairs, p.B * p.H);
+    kern<<<grid, C::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }
 
@@ -389,6 +483,7 @@ int launch_attn_fwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, in
     p.B = s.B; p.L = s.L; p.H = s.H; p.P = s.P; p.Hp = s.H / s.P; p.Lp = s.L / s.P;
     p.layout = layout;
     p.n_tiles = (s.L + kTile - 1) / kTile;
+    p.n_pairs = (p.n_tiles + 1) / 2;
     p.box_rows = layout == ULYSSES_LAYOUT_TOKEN_SHARDED ? gcd_int(p.Lp, kTile) : kTile;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.o = o;
