@@ -13,8 +13,9 @@
 //        S^T  = K Q^T        (M=128 keys, N=64 queries, K=d)
 //        dP^T = V dO^T       (M=128, N=64, K=d)
 //        dV  += P^T dO       (M=128, N=d, K=64)     P^T bf16 in tensor memory (A operand)
-//        dK  += dS^T Q       (M=128, N=d, K=64)     dS^T bf16 written to shared memory
-//        dQ^T = K^T dS^T     (M=d, N=64, K=128)     added into the fp32 accumulator by
+//        dK  += dS^T Q       (M=128, N=d, K=64)     dS^T bf16 in tensor memory (A operand)
+//        dQ^T = K^T dS^T     (M=d, N=64, K=128)     dS^T also in shared memory (B operand);
+//                                                   added into the fp32 accumulator by
 //                                                   bulk reductions from shared memory
 //      Warps: 0 TMA producer (K, V once; Q, dO, lse, Delta per step, 3 stages), 1 MMA
 //      issuer, 2-5 thread-per-key softmax/dS, 6-9 thread-per-feature dQ reduction.
@@ -63,8 +64,8 @@ struct BwdCfg {
     static constexpr uint32_t OFF_BAR = OFF_DQS + 4 * DQS_WARP_BYTES;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
-    // TMEM columns (P^T: 64 bf16 per lane packed in 32 columns)
-    static constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_PT = 192, T_DV = 256, T_DK = 384;
+    // TMEM columns (P^T, dS^T: 64 bf16 per lane packed in 32 columns)
+    static constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_PT = 192, T_DST = 224, T_DV = 256, T_DK = 384;
 };
 
 __device__ __forceinline__ void bwd_coords(const BwdParams& p, int s, int h, int& c1, int& c2, int& c4) {
@@ -266,21 +267,25 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // With d = 64 that block reads the V tile behind K; those lanes of dQ^T are ignored.
             const uint32_t kt_lbo = C::KCHUNK;
 
+            // descriptors at the operands' base addresses; k-steps move them by constant offsets
+            const uint64_t dK_k = sdesc_sw128(aK, 16, 1024), dV_k = sdesc_sw128(aV, 16, 1024);
+            const uint64_t dKt_mn = sdesc_sw128(aK, kt_lbo, 1024), dDSt_mn = sdesc_sw128(aDSt, C::QCHUNK, 1024);
             auto issue_s_dp = [&](int j) {
                 const int st = j % NQ;
-                const uint32_t q = aQ + st * C::QT_BYTES, dO = aDO + st * C::QT_BYTES;
+                const uint64_t dQ_k = sdesc_sw128(aQ + st * C::QT_BYTES, 16, 1024);
+                const uint64_t dDO_k = sdesc_sw128(aDO + st * C::QT_BYTES, 16, 1024);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t ko = (k >> 2) * C::KCHUNK + (k & 3) * 32;
                     const uint32_t qo = (k >> 2) * C::QCHUNK + (k & 3) * 32;
-                    umma_ss(tS, sdesc_sw128(aK + ko, 16, 1024), sdesc_sw128(q + qo, 16, 1024), id_s, k > 0);
+                    umma_ss(tS, sdesc_add(dK_k, ko), sdesc_add(dQ_k, qo), id_s, k > 0);
                 }
                 umma_commit(s_full);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t ko = (k >> 2) * C::KCHUNK + (k & 3) * 32;
                     const uint32_t qo = (k >> 2) * C::QCHUNK + (k & 3) * 32;
-                    umma_ss(tDP, sdesc_sw128(aV + ko, 16, 1024), sdesc_sw128(dO + qo, 16, 1024), id_s, k > 0);
+                    umma_ss(tDP, sdesc_add(dV_k, ko), sdesc_add(dDO_k, qo), id_s, k > 0);
                 }
                 umma_commit(dp_full);
             };
@@ -292,14 +297,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             for (int it = 0; ok && it < n_it; ++it) {
                 const int st = it % NQ;
-                const uint32_t q = aQ + st * C::QT_BYTES, dO = aDO + st * C::QT_BYTES;
+                const uint64_t dQ_mn = sdesc_sw128(aQ + st * C::QT_BYTES, C::QCHUNK, 1024);
+                const uint64_t dDO_mn = sdesc_sw128(aDO + st * C::QT_BYTES, C::QCHUNK, 1024);
                 // dV += P^T dO
                 if (!(ok = mbar_wait(p_full, it & 1, ab, ROLE_MMA, 3))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < kBwdQTile / 16; ++k)  // 16 queries = 8 TMEM columns of P^T
-                    umma_ts(tDV, tmem + C::T_PT + k * 8, sdesc_sw128(dO + k * 2048, C::QCHUNK, 1024), id_kv,
-                            (it > 0 || k > 0) ? 1u : 0u);
+                    umma_ts(tDV, tmem + C::T_PT + k * 8, sdesc_add(dDO_mn, k * 2048), id_kv, (it > 0 || k > 0) ? 1u : 0u);
                 umma_commit(p_free);
                 // next step's S^T and dP^T overlap this step's dS computation
                 if (it + 1 < n_it) {
@@ -314,13 +319,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (it > 0 && !(ok = mbar_wait(dq_free, (it - 1) & 1, ab, ROLE_MMA, 8))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < kBwdQTile / 16; ++k)
-                    umma_ss(tDK, sdesc_sw128(aDSt + k * 32, 16, 1024), sdesc_sw128(q + k * 2048, C::QCHUNK, 1024),
-                            id_kv, (it > 0 || k > 0) ? 1u : 0u);
+                for (int k = 0; k < kBwdQTile / 16; ++k)  // 16 queries = 8 TMEM columns of dS^T
+                    umma_ts(tDK, tmem + C::T_DST + k * 8, sdesc_add(dQ_mn, k * 2048), id_kv, (it > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
                 for (int k = 0; k < kTile / 16; ++k)
-                    umma_ss(tDQ, sdesc_sw128(aK + k * 2048, kt_lbo, 1024), sdesc_sw128(aDSt + k * 2048, C::QCHUNK, 1024),
-                            id_dq, k > 0 ? 1u : 0u);
+                    umma_ss(tDQ, sdesc_add(dKt_mn, k * 2048), sdesc_add(dDSt_mn, k * 2048), id_dq, k > 0 ? 1u : 0u);
                 umma_commit(dq_full);
                 umma_commit(ds_free);
                 umma_commit(qdo_empty + st);
@@ -393,13 +396,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (it - 1) & 1, ab, ROLE_SOFTMAX, 5));
                 if (!ok) break;
             }
+            {
+                uint32_t pk[32];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float* x = dp + u * 8;
-                st_shared_v4(aDSt + sw128_offset(row, u), pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
-                             pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+                for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(dp[2 * i], dp[2 * i + 1]);
+                tmem_st32_u(tmem + C::T_DST + lane_off, pk);  // A operand of dK
+#pragma unroll
+                for (int u = 0; u < 8; ++u)                    // B operand of dQ^T
+                    st_shared_v4(aDSt + sw128_offset(row, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                tmem_wait_st();
             }
             fence_proxy_async_smem();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ds_full);
         }

@@ -252,22 +252,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             bool cur = seq.next(kt, in0, in1);
             // S_t = Q_t K^T for the key tile in K stage sk
             auto issue_s = [&](int t, int sk) {
-                const uint32_t q = aQ + t * C::TILE_BYTES, kb = aK + sk * C::TILE_BYTES;
+                const uint64_t dq = sdesc_sw128(aQ + t * C::TILE_BYTES, 16, 1024);
+                const uint64_t dk = sdesc_sw128(aK + sk * C::TILE_BYTES, 16, 1024);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
-                    umma_ss(tmem + 128 * t, sdesc_sw128(q + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idS,
-                            k > 0 ? 1u : 0u);
+                    umma_ss(tmem + 128 * t, sdesc_add(dq, off), sdesc_add(dk, off), idS, k > 0 ? 1u : 0u);
                 }
                 umma_commit(s_full + t);
             };
             // O_t += P_t V for the value tile in V stage sv
             auto issue_pv = [&](int t, int sv, bool first) {
-                const uint32_t vb = aV + sv * C::TILE_BYTES;
+                const uint64_t dv = sdesc_sw128(aV + sv * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
 #pragma unroll
                 for (int k = 0; k < kTile / 16; ++k)  // 16 keys = 8 TMEM columns of P per step
-                    umma_ts(tmem + 256 + 128 * t, tmem + 128 * t + k * 8,
-                            sdesc_sw128(vb + k * 2048, C::CHUNK_BYTES, 1024), idO, (!first || k > 0) ? 1u : 0u);
+                    umma_ts(tmem + 256 + 128 * t, tmem + 128 * t + k * 8, sdesc_add(dv, k * 2048), idO,
+                            (!first || k > 0) ? 1u : 0u);
             };
             if (cur) {
                 ok = mbar_wait(q_full, 0, ab, ROLE_MMA, 1) && mbar_wait(k_full, 0, ab, ROLE_MMA, 2);

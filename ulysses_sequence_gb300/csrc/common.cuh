@@ -229,6 +229,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
            (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
 
+// The same descriptor with its start address moved by byte_off (a multiple of 16; shared
+// addresses stay far below the 14-bit field's 256 KB range, so no carry leaves the field).
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t byte_off) {
+    return desc + uint64_t(byte_off >> 4);
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane (base lane + i).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     uint32_t* r = reinterpret_cast<uint32_t*>(v);
