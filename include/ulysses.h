@@ -40,7 +40,9 @@
  *     unchanged, NaN payloads included.
  *   - Every wait inside a kernel is bounded (about two seconds). A kernel that runs out
  *     of time records the fact in the device error word and returns early; read it with
- *     ulysses_get_device_status().
+ *     ulysses_get_device_status(). The word holds (kernel << 24) | (role << 16) | site of the
+ *     first wait that gave up: kernel 1 forward, 2 backward, 3 self-test; role 1 loads,
+ *     2 MMA issue, 3 softmax, 4 dQ reduction, 5 epilogue, 6 self-test.
  */
 #ifndef ULYSSES_H
 #define ULYSSES_H
@@ -173,6 +175,14 @@ int ulysses_attn_bwd_noalloc(ulysses_shape_t shape, const ulysses_mask_t *mask, 
 int ulysses_bsmask_build_window_global(int L, int tile, int window_before, int window_after,
                                        int global_stride, int32_t *rowptr, int32_t *kcols,
                                        int32_t *colptr, int32_t *qrows, int *nnz);
+
+/* Health check of the bounded waits: enqueues one small kernel whose two waiting warps wait
+ * on an mbarrier that nothing ever arrives on. They give up after the same limit as the
+ * attention kernels (about two seconds), record ULYSSES_ERR_DEVICE_TIMEOUT in the device error
+ * word and return, leaving the context usable. The next ulysses_get_device_status then
+ * reports ULYSSES_ERR_DEVICE_TIMEOUT with detail (3 << 24) | (6 << 16) | site, site 1 or 2
+ * (whichever warp ran out first). Returns ULYSSES_ERR_CUDA if the launch fails. */
+int ulysses_selftest_timeout(void *stream);
 
 /* Synchronises `stream`, then reads and clears the current device's error word.
  * Returns ULYSSES_OK, ULYSSES_ERR_DEVICE_TIMEOUT (a bounded wait ran out), or

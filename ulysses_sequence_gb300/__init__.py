@@ -37,7 +37,7 @@ class MaskStruct(ctypes.Structure):
 
 EXPORTS = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_attn_fwd", "ulysses_attn_bwd_workspace_size",
            "ulysses_attn_bwd", "ulysses_attn_bwd_noalloc", "ulysses_bsmask_build_window_global",
-           "ulysses_get_device_status", "ulysses_status_string")
+           "ulysses_get_device_status", "ulysses_selftest_timeout", "ulysses_status_string")
 BWD_NOALLOC_SCRATCH_BYTES = 96 * 1024 * 1024  # ULYSSES_BWD_NOALLOC_SCRATCH_BYTES
 
 _lib = None
@@ -64,6 +64,7 @@ def load() -> ctypes.CDLL:
     ip = ctypes.POINTER(ctypes.c_int32)
     lib.ulysses_bsmask_build_window_global.argtypes = [i, i, i, i, i, ip, ip, ip, ip, ctypes.POINTER(ctypes.c_int)]
     lib.ulysses_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.ulysses_selftest_timeout.argtypes = [vp]
     lib.ulysses_status_string.argtypes = [i]
     lib.ulysses_status_string.restype = ctypes.c_char_p
     for name in EXPORTS:
@@ -135,6 +136,10 @@ def ulysses_get_device_status(stream: int) -> Tuple[int, int]:
     detail = ctypes.c_uint32(0)
     rc = load().ulysses_get_device_status(stream, ctypes.byref(detail))
     return rc, detail.value
+
+
+def ulysses_selftest_timeout(stream: int) -> int:
+    return load().ulysses_selftest_timeout(stream)
 
 
 def ulysses_status_string(status: int) -> str:

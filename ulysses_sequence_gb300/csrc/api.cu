@@ -127,6 +127,25 @@ int validate_attn(const ulysses_shape_t& s, const ulysses_mask_t* mask, int layo
 float resolve_scale(float scale, int d) { return scale > 0.f ? scale : 1.0f / sqrtf(float(d)); }
 
 }  // namespace
+
+// Two warps wait on an mbarrier that nothing ever arrives on, through the same bounded wait
+// the attention kernels use: the first to run out of time records the error word and sets
+// the CTA's abort flag, the other sees the flag (or runs out too), and both return.
+__global__ void selftest_timeout_kernel(uint32_t* err) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const Abort ab{&abort_flag, err, KID_SELFTEST};
+    if ((threadIdx.x & 31) == 0) mbar_wait(&bar, 0, ab, ROLE_SELFTEST, 1 + threadIdx.x / 32);
+    __syncwarp();
+    __syncthreads();
+}
+
 }  // namespace ulysses
 
 using namespace ulysses;
@@ -241,6 +260,13 @@ int ulysses_bsmask_build_window_global(int L, int tile, int window_before, int w
     for (int qt = 0; qt < n; ++qt)
         for (int e = rp[qt]; e < rp[qt + 1]; ++e) qrows[pos[cols[e]]++] = qt;
     return ULYSSES_OK;
+}
+
+int ulysses_selftest_timeout(void* stream) {
+    uint32_t* err = device_error_word();
+    if (!err) return ULYSSES_ERR_CUDA;
+    selftest_timeout_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(err);
+    return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }
 
 int ulysses_get_device_status(void* stream, uint32_t* detail) {

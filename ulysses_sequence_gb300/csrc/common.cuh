@@ -16,8 +16,8 @@ namespace ulysses {
 //   bits 31..24 kernel id, 23..16 role, 15..0 wait site.
 // ---------------------------------------------------------------------------------------
 
-enum : uint32_t { KID_FWD = 1, KID_BWD = 2 };
-enum : uint32_t { ROLE_LOAD = 1, ROLE_MMA = 2, ROLE_SOFTMAX = 3, ROLE_DQ = 4, ROLE_EPI = 5 };
+enum : uint32_t { KID_FWD = 1, KID_BWD = 2, KID_SELFTEST = 3 };
+enum : uint32_t { ROLE_LOAD = 1, ROLE_MMA = 2, ROLE_SOFTMAX = 3, ROLE_DQ = 4, ROLE_EPI = 5, ROLE_SELFTEST = 6 };
 
 // A wait gives up after this many nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
