@@ -224,3 +224,54 @@ def test_large_workload_sampled_rows(name, heads):
     for s in stats.values():
         s.check()
     assert lse_err <= LSE_MAX_ABS, lse_err
+
+
+GUARD = 4096
+
+
+def _guarded(shape, dtype):
+    """A tensor of `shape` in the middle of a buffer whose both ends hold a canary pattern."""
+    n = int(np.prod(shape))
+    elem = torch.int16 if dtype == torch.bfloat16 else torch.int32
+    buf = torch.full((n + 2 * GUARD,), 0x5A5A, dtype=elem, device="cuda")
+    return buf, buf[GUARD:GUARD + n].view(dtype).view(shape)
+
+
+def _guards_intact(buf):
+    h = buf.cpu()
+    return bool((h[:GUARD] == 0x5A5A).all() and (h[-GUARD:] == 0x5A5A).all())
+
+
+@pytest.mark.parametrize("B,L,H,d,P,kind,layout", [(1, 320, 4, 128, 4, "causal", U.LAYOUT_TOKEN_SHARDED),
+                                                    (1, 300, 6, 64, 3, "none", U.LAYOUT_HEAD_SHARDED),
+                                                    (2, 640, 4, 128, 2, "tiles", U.LAYOUT_TOKEN_SHARDED)])
+def test_attention_writes_stay_inside_outputs(B, L, H, d, P, kind, layout):
+    """Ragged tails, both layouts and block-sparse lists: every output and the workspace are
+    surrounded by canaries, which must be untouched after forward and backward."""
+    t = workloads.draw(B, L, H, d, P, seed=31)
+    if layout == U.LAYOUT_HEAD_SHARDED:
+        dev = {n: U.seq_to_head(x.cuda(), P) for n, x in t.items()}
+    else:
+        dev = {n: x.cuda() for n, x in t.items()}
+    tiles = oracle.window_global_tiles(-(-L // 128), 1, 0, 3) if kind == "tiles" else None
+    mask = gpu_mask(kind, L, tiles)
+    shape = dev["q"].shape
+    bufs = {}
+    bufs["o"], o = _guarded(shape, torch.bfloat16)
+    bufs["lse"], lse = _guarded((P, B, H // P, L), torch.float32)
+    bufs["dq"], dq = _guarded(shape, torch.bfloat16)
+    bufs["dk"], dk = _guarded(shape, torch.bfloat16)
+    bufs["dv"], dv = _guarded(shape, torch.bfloat16)
+    ws_bytes = U.ulysses_attn_bwd_workspace_size(U.token_shape(t["q"], P))
+    ws_buf = torch.full((ws_bytes + 2 * GUARD * 64,), 0x5A, dtype=torch.uint8, device="cuda")
+    ws = ws_buf[GUARD * 64:GUARD * 64 + ws_bytes]
+    U.attn_fwd(dev["q"], dev["k"], dev["v"], P, mask, layout, o=o, lse=lse)
+    U.attn_bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], P, mask, layout, dq=dq, dk=dk, dv=dv, workspace=ws)
+    torch.cuda.synchronize()
+    assert U.device_status()[0] == U.OK
+    for name, buf in bufs.items():
+        assert _guards_intact(buf), name
+    wh = ws_buf.cpu()
+    assert bool((wh[:GUARD * 64] == 0x5A).all() and (wh[-GUARD * 64:] == 0x5A).all()), "workspace"
+    for x in (o, dq, dk, dv):
+        assert torch.isfinite(x.float()).all()
