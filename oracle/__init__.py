@@ -63,6 +63,10 @@ def _load():
                 f = getattr(lib, fn)
                 f.restype = ctypes.c_int
                 f.argtypes = [i64, i64, i64, i64, i64, i64, ctypes.c_void_p, ctypes.c_void_p]
+            lib.oracle_kv_seq_to_head.restype = ctypes.c_int
+            lib.oracle_kv_seq_to_head.argtypes = [i64, i64, i64, i64, i64, i64, ctypes.c_void_p, ctypes.c_void_p]
+            lib.oracle_kv_head_to_seq_sum.restype = ctypes.c_int
+            lib.oracle_kv_head_to_seq_sum.argtypes = [i64, i64, i64, i64, i64, ctypes.c_void_p, ctypes.c_void_p]
             lib.oracle_bf16_to_f64.restype = None
             lib.oracle_bf16_to_f64.argtypes = [i64, ctypes.c_void_p, ctypes.c_void_p]
             _lib = lib
@@ -98,6 +102,38 @@ def head_to_seq(y: np.ndarray, P: int) -> np.ndarray:
     rc = _load().oracle_head_to_seq(P, B, L, H, d, y.itemsize, _ptr(y), _ptr(z))
     if rc != 0:
         raise ValueError("oracle_head_to_seq rejected the shape")
+    return z
+
+
+def kv_heads_per_rank(Hkv: int, P: int) -> int:
+    """K/V heads each head group holds: Hkv/P, or 1 when P > Hkv (heads replicated)."""
+    if Hkv % P == 0:
+        return Hkv // P
+    if P % Hkv == 0:
+        return 1
+    raise ValueError("need Hkv % P == 0 or P % Hkv == 0")
+
+
+def kv_seq_to_head(x: np.ndarray, P: int) -> np.ndarray:
+    """Token-sharded K/V [P][B][Lp][Hkv][d] -> head-sharded [P][B][L][Hkvp][d] (C loops)."""
+    x = np.ascontiguousarray(x)
+    P_, B, Lp, Hkv, d = x.shape
+    assert P_ == P
+    Hkvp = kv_heads_per_rank(Hkv, P)
+    y = np.empty((P, B, Lp * P, Hkvp, d), dtype=x.dtype)
+    if _load().oracle_kv_seq_to_head(P, B, Lp * P, Hkv, d, x.itemsize, _ptr(x), _ptr(y)) != 0:
+        raise ValueError("oracle_kv_seq_to_head rejected the shape")
+    return y
+
+
+def kv_head_to_seq_sum(y: np.ndarray, P: int, Hkv: int) -> np.ndarray:
+    """Adjoint of kv_seq_to_head on fp64 gradients: sums the replicas of each K/V head."""
+    y = np.ascontiguousarray(y, dtype=np.float64)
+    P_, B, L, Hkvp, d = y.shape
+    assert P_ == P and Hkvp == kv_heads_per_rank(Hkv, P)
+    z = np.empty((P, B, L // P, Hkv, d))
+    if _load().oracle_kv_head_to_seq_sum(P, B, L, Hkv, d, _ptr(y), _ptr(z)) != 0:
+        raise ValueError("oracle_kv_head_to_seq_sum rejected the shape")
     return z
 
 
@@ -226,50 +262,59 @@ def attention_full(q_tok: np.ndarray, k_tok: np.ndarray, v_tok: np.ndarray, P: i
                    do_tok: Optional[np.ndarray] = None, scale: Optional[float] = None) -> Dict[str, np.ndarray]:
     """The whole attention block on token-sharded inputs, every row.
 
-    Inputs are bf16 bit patterns (uint16) or fp64 arrays, [P][B][Lp][H][d].
-    Steps: seq->head relayout of Q, K, V (and dO); per head group and head, exact
-    attention over the full sequence (and its gradient); head->seq relayout of O (and
-    dQ, dK, dV). Returns fp64 "o" (and "dq", "dk", "dv") [P][B][Lp][H][d] and "lse"
-    [P][B][Hp][L].
+    Inputs are bf16 bit patterns (uint16) or fp64 arrays: Q (and dO) [P][B][Lp][H][d], K and V
+    [P][B][Lp][Hkv][d] with H % Hkv == 0 (Hkv == H is plain multi-head attention).
+    Steps: seq->head relayout of Q (and dO) and of K, V (kv_seq_to_head); per head group and
+    query head h, exact attention over the full sequence against K/V head h // (H/Hkv) (and its
+    gradient); head->seq relayout of O, dQ, and the summing adjoint for dK, dV. Returns fp64
+    "o" (and "dq", "dk", "dv") in the token layout and "lse" [P][B][Hp][L].
     """
-    tensors = {"q": q_tok, "k": k_tok, "v": v_tok}
+    head = {"q": seq_to_head(q_tok, P), "k": kv_seq_to_head(k_tok, P), "v": kv_seq_to_head(v_tok, P)}
     if do_tok is not None:
-        tensors["do"] = do_tok
-    head = {}
-    for nme, t in tensors.items():
-        y = seq_to_head(t, P)
-        head[nme] = bf16_to_f64(y) if y.dtype == np.uint16 else y.astype(np.float64)
+        head["do"] = seq_to_head(do_tok, P)
+    head = {n: bf16_to_f64(y) if y.dtype == np.uint16 else y.astype(np.float64) for n, y in head.items()}
     _, B, L, Hp, d = head["q"].shape
+    Hkv = k_tok.shape[3]
+    H = Hp * P
+    G = H // Hkv
+    Hkvp = head["k"].shape[3]
     sc = 1.0 / np.sqrt(d) if scale is None else scale
     o = np.zeros((P, B, L, Hp, d))
     lse = np.zeros((P, B, Hp, L))
-    grads = {nme: np.zeros((P, B, L, Hp, d)) for nme in ("dq", "dk", "dv")} if do_tok is not None else {}
+    grads = {}
+    if do_tok is not None:
+        grads = {"dq": np.zeros((P, B, L, Hp, d)), "dk": np.zeros((P, B, L, Hkvp, d)),
+                 "dv": np.zeros((P, B, L, Hkvp, d))}
     rows = np.arange(L)
     for g in range(P):
         for b in range(B):
             for j in range(Hp):
-                qh, kh, vh = (_head_view(head[x], g, b, j) for x in ("q", "k", "v"))
+                h = g * Hp + j
+                jk = h // G - g * Hkvp if Hkv >= P else 0
+                qh = head["q"][g, b, :, j, :]
+                kh, vh = head["k"][g, b, :, jk, :], head["v"][g, b, :, jk, :]
                 O, LSE = head_forward(qh, kh, vh, rows, mask, sc)
                 o[g, b, :, j, :] = O
                 lse[g, b, j, :] = LSE
                 if do_tok is not None:
-                    dQ, dK, dV = head_backward(qh, kh, vh, _head_view(head["do"], g, b, j), O, LSE,
-                                               rows, mask, sc)
+                    dQ, dK, dV = head_backward(qh, kh, vh, head["do"][g, b, :, j, :], O, LSE, rows, mask, sc)
                     grads["dq"][g, b, :, j, :] = dQ
-                    grads["dk"][g, b, :, j, :] = dK
-                    grads["dv"][g, b, :, j, :] = dV
+                    grads["dk"][g, b, :, jk, :] += dK
+                    grads["dv"][g, b, :, jk, :] += dV
     out = {"o": head_to_seq(o, P), "lse": lse}
-    for nme, t in grads.items():
-        out[nme] = head_to_seq(t, P)
+    if grads:
+        out["dq"] = head_to_seq(grads["dq"], P)
+        out["dk"] = kv_head_to_seq_sum(grads["dk"], P, Hkv)
+        out["dv"] = kv_head_to_seq_sum(grads["dv"], P, Hkv)
     return out
 
 
 def _sampled_task(task):
     """One (batch, head) of the sampled mode; runs in the caller or in a pool worker."""
-    b, h, rows, heads, mask, sc = task
+    b, h, kvh, rows, heads, mask, sc = task
     conv = {nme: bf16_to_f64(x) if x.dtype == np.uint16 else x.astype(np.float64) for nme, x in heads.items()}
     O, LSE = head_forward(conv["q"], conv["k"], conv["v"], rows, mask, sc)
-    res = {"b": b, "h": h, "rows": rows, "o": O, "lse": LSE}
+    res = {"b": b, "h": h, "kvh": kvh, "rows": rows, "o": O, "lse": LSE}
     if "do" in conv:
         dQ, dK, dV = head_backward(conv["q"], conv["k"], conv["v"], conv["do"][rows], O, LSE, rows, mask, sc)
         res.update(dq=dQ, dk=dK, dv=dV)
@@ -281,21 +326,24 @@ _BLAS_VARS = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
 
 def attention_sampled(q_tok, k_tok, v_tok, do_tok, P: int, mask: Mask, rows_bi: np.ndarray,
                       scale: Optional[float] = None, heads=None, workers: int = 0) -> Iterator[dict]:
-    """Per-(batch, head) results on sampled query rows, for workloads too large to do whole.
+    """Per-(batch, query head) results on sampled query rows, for workloads too large to do whole.
 
-    rows_bi: int [n, 2] of (b, i). For each (b, head) yields a dict with
-      "b", "h", "rows" (sequence indices i), "o" [n_b, d], "lse" [n_b], and, when do_tok is
-      given, "dq" [n_b, d] and "dk", "dv" [L, d]: the gradient contributions of the sampled
-      rows (equal to the full dK, dV of a pass whose dO is zero on every other row).
+    rows_bi: int [n, 2] of (b, i). For each (b, h) yields a dict with "b", "h", "kvh" (the K/V
+      head it attends with, h // (H/Hkv)), "rows" (sequence indices i), "o" [n_b, d], "lse"
+      [n_b], and, when do_tok is given, "dq" [n_b, d] and "dk", "dv" [L, d]: this query head's
+      sampled rows' gradient contributions to K/V head kvh (summing them over the query heads
+      of a group gives what a pass whose dO is zero on every other row produces).
     (batch, head) pairs are independent; with workers > 1 they are spread over a process
     pool started with "spawn" (results arrive in the same order).
     """
-    head = {}
-    for nme, t in (("q", q_tok), ("k", k_tok), ("v", v_tok), ("do", do_tok)):
-        if t is not None:
-            head[nme] = seq_to_head(t, P)
+    head = {"q": seq_to_head(q_tok, P), "k": kv_seq_to_head(k_tok, P), "v": kv_seq_to_head(v_tok, P)}
+    if do_tok is not None:
+        head["do"] = seq_to_head(do_tok, P)
     _, B, L, Hp, d = head["q"].shape
     H = Hp * P
+    Hkv = k_tok.shape[3]
+    G = H // Hkv
+    Hkvp = head["k"].shape[3]
     sc = 1.0 / np.sqrt(d) if scale is None else scale
 
     def tasks():
@@ -305,8 +353,11 @@ def attention_sampled(q_tok, k_tok, v_tok, do_tok, P: int, mask: Mask, rows_bi: 
                 continue
             for h in (range(H) if heads is None else heads):
                 g, j = divmod(h, Hp)
-                yield (b, h, rows, {nme: np.ascontiguousarray(_head_view(y, g, b, j)) for nme, y in head.items()},
-                       mask, sc)
+                jk = h // G - g * Hkvp if Hkv >= P else 0
+                views = {"q": head["q"][g, b, :, j, :], "k": head["k"][g, b, :, jk, :], "v": head["v"][g, b, :, jk, :]}
+                if "do" in head:
+                    views["do"] = head["do"][g, b, :, j, :]
+                yield (b, h, h // G, rows, {n: np.ascontiguousarray(x) for n, x in views.items()}, mask, sc)
 
     if workers <= 1:
         for task in tasks():

@@ -90,3 +90,70 @@ void oracle_bf16_to_f64(int64_t n, const uint16_t *in, double *out)
         out[i] = (double)f;
     }
 }
+
+/*
+ * Grouped K/V heads (GQA/MQA): K and V carry Hkv heads shared by groups of H/Hkv query heads
+ * (paper summary section 6, "Architecture generalization to grouped-query and multi-query
+ * attention"; pinyu.ai page, "Head-count constraints"). Two regimes:
+ *   Hkv % P == 0: receiver g gets the contiguous K/V heads [g*Hkv/P, (g+1)*Hkv/P), just as for Q;
+ *   P % Hkv == 0: every receiver gets one K/V head, head g / (P/Hkv): each head is replicated
+ *                 on P/Hkv receivers (the replication the pinyu.ai page mentions).
+ * Head-sharded K/V: [P][B][L][Hkvp][d] with Hkvp = Hkv/P or 1.
+ * Returns 1 for shapes outside both regimes.
+ */
+static int kv_shape(int64_t P, int64_t Hkv, int64_t *Hkvp, int64_t *rep)
+{
+    if (P <= 0 || Hkv <= 0) return 0;
+    if (Hkv % P == 0) { *Hkvp = Hkv / P; *rep = 1; return 1; }
+    if (P % Hkv == 0) { *Hkvp = 1; *rep = P / Hkv; return 1; }
+    return 0;
+}
+
+/* source K/V head of slot j on receiver g */
+static int64_t kv_source_head(int64_t g, int64_t j, int64_t Hkvp, int64_t rep)
+{
+    return rep == 1 ? g * Hkvp + j : g / rep;
+}
+
+/* Y[g][b][s][j][e] = X[s / Lp][b][s % Lp][kv_source_head(g, j)][e]; loops over the destination. */
+int oracle_kv_seq_to_head(int64_t P, int64_t B, int64_t L, int64_t Hkv, int64_t d, int64_t elem_bytes,
+                          const void *x, void *y)
+{
+    int64_t Hkvp, rep;
+    if (!kv_shape(P, Hkv, &Hkvp, &rep) || !shape_ok(P, B, L, P, d, elem_bytes)) return 1;
+    const int64_t Lp = L / P;
+    const char *X = (const char *)x;
+    char *Y = (char *)y;
+    for (int64_t g = 0; g < P; ++g)
+        for (int64_t b = 0; b < B; ++b)
+            for (int64_t s = 0; s < L; ++s)
+                for (int64_t j = 0; j < Hkvp; ++j)
+                    for (int64_t e = 0; e < d; ++e) {
+                        const int64_t hs = kv_source_head(g, j, Hkvp, rep);
+                        const int64_t src = (((s / Lp * B + b) * Lp + s % Lp) * Hkv + hs) * d + e;
+                        const int64_t dst = (((g * B + b) * L + s) * Hkvp + j) * d + e;
+                        move_one(Y + dst * elem_bytes, X + src * elem_bytes, elem_bytes);
+                    }
+    return 0;
+}
+
+/* The adjoint of oracle_kv_seq_to_head on fp64 values (used for dK, dV):
+ *   Z[r][b][t][h][e] = sum over (g, j) with kv_source_head(g, j) == h of Y[g][b][r*Lp + t][j][e].
+ * Without replication every head has exactly one source and this is the inverse permutation. */
+int oracle_kv_head_to_seq_sum(int64_t P, int64_t B, int64_t L, int64_t Hkv, int64_t d, const double *y, double *z)
+{
+    int64_t Hkvp, rep;
+    if (!kv_shape(P, Hkv, &Hkvp, &rep) || L % P != 0 || B < 0 || d <= 0) return 1;
+    const int64_t Lp = L / P;
+    for (int64_t i = 0; i < P * B * Lp * Hkv * d; ++i) z[i] = 0.0;
+    for (int64_t g = 0; g < P; ++g)
+        for (int64_t b = 0; b < B; ++b)
+            for (int64_t s = 0; s < L; ++s)
+                for (int64_t j = 0; j < Hkvp; ++j)
+                    for (int64_t e = 0; e < d; ++e) {
+                        const int64_t hs = kv_source_head(g, j, Hkvp, rep);
+                        const int64_t dst = (((s / Lp * B + b) * Lp + s % Lp) * Hkv + hs) * d + e;
+                        z[dst] += y[(((g * B + b) * L + s) * Hkvp + j) * d + e];
+                    }
+    return 0;
+}

@@ -321,3 +321,75 @@ def test_golden_block_sparse_tile_counts():
     for L, tile, wb, wa, gs, active, total in ((int(x) for x in r) for r in rows):
         t = oracle.window_global_tiles(L // tile, wb, wa, gs)
         assert int(t.sum()) == active and t.size == total
+
+
+# ----------------------------------------------------------------------------- grouped K/V heads
+
+GQA = [(2, 8, 2), (4, 8, 2), (4, 8, 1), (8, 8, 4), (2, 4, 4)]  # (P, H, Hkv): both regimes, MQA, MHA
+
+
+@pytest.mark.parametrize("P,H,Hkv", GQA)
+def test_kv_relayout_receiver_rule(P, H, Hkv):
+    B, L, d = 2, 16, 3
+    Lp = L // P
+    r, b, t, h, e = np.meshgrid(np.arange(P), np.arange(B), np.arange(Lp), np.arange(Hkv), np.arange(d), indexing="ij")
+    code = ((((r * B + b) * Lp + t) * Hkv + h) * d + e).astype(np.int64)
+    y = oracle.kv_seq_to_head(code, P)
+    Hkvp = Hkv // P if Hkv % P == 0 else 1
+    assert y.shape == (P, B, L, Hkvp, d)
+    g, b2, s, j, e2 = np.meshgrid(np.arange(P), np.arange(B), np.arange(L), np.arange(Hkvp), np.arange(d), indexing="ij")
+    # receiver g holds K/V heads [g*Hkv/P, ...) or, replicated, head floor(g*Hkv/P)
+    src_head = g * Hkvp + j if Hkv % P == 0 else (g * Hkv) // P
+    want = (((s // Lp) * B + b2) * Lp + s % Lp) * Hkv * d + src_head * d + e2
+    assert np.array_equal(y, want)
+    if Hkv % P == 0:
+        assert np.array_equal(y, oracle.seq_to_head(code, P))
+
+
+@pytest.mark.parametrize("P,H,Hkv", GQA)
+def test_kv_relayout_adjoint_identity(P, H, Hkv):
+    """<y, R x> == <R^T y, x> for the relayout R and its summing adjoint R^T."""
+    B, L, d = 2, 8, 4
+    x = RNG.standard_normal((P, B, L // P, Hkv, d))
+    Hkvp = Hkv // P if Hkv % P == 0 else 1
+    y = RNG.standard_normal((P, B, L, Hkvp, d))
+    lhs = np.sum(y * oracle.kv_seq_to_head(x, P))
+    rhs = np.sum(oracle.kv_head_to_seq_sum(y, P, Hkv) * x)
+    assert abs(lhs - rhs) <= 1e-12 * max(1.0, abs(lhs))
+
+
+def repeat_kv(x_tok, G):
+    """[P][B][Lp][Hkv][d] -> [P][B][Lp][Hkv*G][d], each K/V head repeated for its G query heads."""
+    return np.repeat(x_tok, G, axis=3)
+
+
+@pytest.mark.parametrize("P,H,Hkv", GQA)
+@pytest.mark.parametrize("kind", ["causal", "none"])
+def test_gqa_equals_mha_on_repeated_heads(P, H, Hkv, kind):
+    B, L, d = 1, 16, 8
+    G = H // Hkv
+    q, do = rand_tok(P, B, L, H, d), rand_tok(P, B, L, H, d)
+    k, v = rand_tok(P, B, L, Hkv, d), rand_tok(P, B, L, Hkv, d)
+    gqa = oracle.attention_full(q, k, v, P, Mask(kind), do_tok=do)
+    mha = oracle.attention_full(q, repeat_kv(k, G), repeat_kv(v, G), P, Mask(kind), do_tok=do)
+    for n in ("o", "lse", "dq"):
+        np.testing.assert_allclose(gqa[n], mha[n], rtol=0, atol=1e-13)
+    for n in ("dk", "dv"):
+        summed = mha[n].reshape(P, B, L // P, Hkv, G, d).sum(axis=4)
+        np.testing.assert_allclose(gqa[n], summed, rtol=0, atol=1e-12)
+
+
+@pytest.mark.skipif(
+    "enable_gqa" not in torch.nn.functional.scaled_dot_product_attention.__doc__, reason="torch without enable_gqa")
+@pytest.mark.parametrize("P,H,Hkv", [(2, 8, 2), (4, 8, 1)])
+def test_gqa_matches_torch_sdpa(P, H, Hkv):
+    B, L, d = 2, 16, 8
+    q, do = rand_tok(P, B, L, H, d), rand_tok(P, B, L, H, d)
+    k, v = rand_tok(P, B, L, Hkv, d), rand_tok(P, B, L, Hkv, d)
+    g = oracle.attention_full(q, k, v, P, Mask("causal"), do_tok=do)
+    tq, tk, tv = (torch.from_numpy(logical(x)).permute(0, 2, 1, 3).requires_grad_(True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True, enable_gqa=True)
+    o.backward(torch.from_numpy(logical(do)).permute(0, 2, 1, 3))
+    np.testing.assert_allclose(logical(g["o"]), o.detach().permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-12)
+    for name, t in (("dq", tq), ("dk", tk), ("dv", tv)):
+        np.testing.assert_allclose(logical(g[name]), t.grad.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-11)
