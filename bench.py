@@ -279,7 +279,7 @@ def main():
     f_fwd, f_bwd = flops(w)
     total_flops = f_fwd + f_bwd
 
-    t = workloads.draw(w.B, w.L, w.H, w.d, w.P, w.seed + 1000 * rank, q_scale=w.q_scale)
+    t = workloads.draw(w.B, w.L, w.H, w.d, w.P, w.seed + 1000 * rank, q_scale=w.q_scale, H_kv=w.H_kv)
     host = {n: x.pin_memory() for n, x in t.items()}
     x = {n: v.to(dev) for n, v in host.items()}
     mask = U.Mask.causal() if w.mask == "causal" else (
@@ -400,13 +400,16 @@ def main():
 
     if rank == 0:
         pairs = permitted_pairs(w)
-        comm = 4 * w.B * w.L * w.H * w.d * 2 // w.P
+        # Q and O with H heads, K and V with Hkv (each head group receives Hkv/P heads, or one
+        # copy when P > Hkv): 4Nh/P for multi-head attention
+        kv_per_group = w.Hkv // w.P if w.Hkv % w.P == 0 else 1
+        comm = (2 * w.H + 2 * kv_per_group * w.P) * w.B * w.L * w.d * 2 // w.P
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "d_h": w.d, "P": w.P, "mask": w.mask,
-                       "passes": "fwd+bwd" if w.backward else "fwd", "layout": "token-sharded (relayouts fused)",
+            "config": {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "H_kv": w.Hkv, "d_h": w.d, "P": w.P,
+                       "mask": w.mask, "passes": "fwd+bwd" if w.backward else "fwd", "layout": "token-sharded (relayouts fused)",
                        "l2": "inputs larger than L2 (4 x %.0f MB bf16)" % (x["q"].numel() * 2 / 1e6),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "frac_of_peak": value / world / peak_tf,

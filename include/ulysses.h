@@ -22,6 +22,9 @@
  *   ULYSSES_LAYOUT_TOKEN_SHARDED  [P][B][Lp][H][d_h]   (shard r = one rank's tensor)
  *   ULYSSES_LAYOUT_HEAD_SHARDED   [P][B][L][Hp][d_h]   (group g = one rank's tensor)
  *   log-sum-exp (fp32, natural log of the scaled scores)  [P][B][Hp][L]
+ * Key/value tensors (K, V, dK, dV) have H_kv heads in place of H: token-sharded
+ * [P][B][Lp][H_kv][d_h], head-sharded [P][B][L][Hkvp][d_h] with Hkvp = H_kv / P, or 1 when
+ * P > H_kv (group g then holds a copy of key/value head g / (P / H_kv)).
  *
  * Conventions for every call below:
  *   - Ownership: the caller allocates and owns every buffer. The library allocates no
@@ -74,11 +77,18 @@ typedef enum {
     ULYSSES_MASK_BLOCK_SPARSE = 2   /* whole tile x tile blocks from the lists below    */
 } ulysses_mask_kind_t;
 
-/* Shape of one attention block: batch B, sequence L (the paper's N), H heads of width
+/* Shape of one attention block: batch B, sequence L (the paper's N), H query heads of width
  * d_h, P shards. Requires H % P == 0 and L % P == 0 (the head cut and the token cut must
- * be even; pinyu.ai page, "Head-count constraints"). */
+ * be even; pinyu.ai page, "Head-count constraints").
+ * H_kv: number of key/value heads (grouped-query attention; the pinyu.ai page's head-count
+ * constraints and the paper summary's discussion of GQA/MQA). 0 means H (multi-head
+ * attention). Query head h attends with key/value head h / (H / H_kv). Requires
+ * H % H_kv == 0 and either H_kv % P == 0 (each head group receives H_kv / P whole
+ * key/value heads) or P % H_kv == 0 (each head group receives one key/value head, replicated
+ * on P / H_kv groups). */
 typedef struct {
     int B, L, H, d_h, P;
+    int H_kv;
 } ulysses_shape_t;
 
 /* Attention mask. For ULYSSES_MASK_BLOCK_SPARSE (a sparsity pattern applied locally after
@@ -112,11 +122,29 @@ int ulysses_seq_to_head(ulysses_shape_t shape, const void *in, void *out, void *
  *   out[r][b][t][h][e] = in[h / Hp][b][r * Lp + t][h % Hp][e]. */
 int ulysses_head_to_seq(ulysses_shape_t shape, const void *in, void *out, void *stream);
 
+/* Key/value sequence-to-head relayout, the first all-to-all applied to K or V with H_kv
+ * heads (the seq->head relayout above with the receiver rule for grouped key/value heads):
+ *   out[g][b][s][j][e] = in[s / Lp][b][s % Lp][src(g, j)][e],
+ *   src(g, j) = g * Hkvp + j when H_kv % P == 0, else g / (P / H_kv) (replicated).
+ * in: [P][B][Lp][H_kv][d_h], out: [P][B][L][Hkvp][d_h], 16-bit elements moved unchanged.
+ * Only B, L, d_h, P and H_kv (H when H_kv is 0) are used: it needs L % P == 0 and
+ * H_kv % P == 0 or P % H_kv == 0, but not H % P == 0. With H_kv == H it equals
+ * ulysses_seq_to_head. */
+int ulysses_kv_seq_to_head(ulysses_shape_t shape, const void *in, void *out, void *stream);
+
+/* Adjoint of ulysses_kv_seq_to_head, for head-sharded key/value gradients: every key/value
+ * head receives the sum over its copies,
+ *   out[r][b][t][h][e] = sum over (g, j) with src(g, j) == h of in[g][b][r * Lp + t][j][e].
+ * bf16 in and out; the sum is formed in fp32 in ascending g and rounded to nearest-even.
+ * Without replication each head has one copy and this is the exact inverse permutation. */
+int ulysses_kv_head_to_seq_sum(ulysses_shape_t shape, const void *in, void *out, void *stream);
+
 /* Attention forward for every head group (paper summary section 3.4.1 "The challenge at
  * the attention boundary", pinyu.ai page "The layout that saves memory breaks at
  * attention"):  S = scale * Q K^T + mask,  O = softmax(S) V,  lse = ln sum exp(S).
- * q, k, v, o: bf16 in io_layout; with TOKEN_SHARDED the two relayouts are fused into the
- * kernel's loads and stores, so o comes back token-sharded. lse: fp32 [P][B][Hp][L].
+ * q, k, v, o: bf16 in io_layout (k, v with H_kv heads); with TOKEN_SHARDED the two relayouts
+ * are fused into the kernel's loads and stores, so o comes back token-sharded.
+ * lse: fp32 [P][B][Hp][L].
  * softmax_scale <= 0 selects 1/sqrt(d_h). A row with no permitted key gets O = 0 and
  * lse = -inf.
  * Supported: d_h in {64, 128}. TOKEN_SHARDED additionally needs Lp % 8 == 0. Any L >= 1
@@ -133,7 +161,10 @@ size_t ulysses_attn_bwd_workspace_size(ulysses_shape_t shape);
  * it out). With P = exp(S - lse) on permitted pairs, Delta = rowsum(dO * O):
  *   dV = P^T dO,  dS = P * (dO V^T - Delta),  dQ = scale dS K,  dK = scale dS^T Q.
  * q, k, v, o, dO, dq, dk, dv: bf16 in io_layout (TOKEN_SHARDED fuses the relayout of dO
- * in and of dq, dk, dv out); lse as written by ulysses_attn_fwd. workspace: at least
+ * in and of dq, dk, dv out; k, v, dk, dv with H_kv heads); lse as written by
+ * ulysses_attn_fwd. With grouped key/value heads, dk and dv hold the sum over the query heads
+ * of each group; with HEAD_SHARDED and replicated key/value heads (P > H_kv), each group's
+ * copy receives its own query heads' part, and ulysses_kv_head_to_seq_sum adds the copies. workspace: at least
  * ulysses_attn_bwd_workspace_size(shape) bytes, 256-byte aligned, caller-owned, contents
  * need not be initialised. dq accumulates in fp32 with atomic adds, so its bits may vary
  * from run to run by fp32 rounding; dk and dv are deterministic. */

@@ -48,7 +48,8 @@ class ErrStats:
 
     def check(self, max_abs=MAX_ABS, rel_l2=REL_L2):
         assert self.n > 0, self.name
-        assert self.max_abs <= max_abs, f"{self.name}: max-abs {self.max_abs:.3e} > {max_abs}"
+        if max_abs is not None:
+            assert self.max_abs <= max_abs, f"{self.name}: max-abs {self.max_abs:.3e} > {max_abs}"
         if rel_l2 is not None:
             assert self.rel_l2 <= rel_l2, f"{self.name}: rel-L2 {self.rel_l2:.3e} > {rel_l2}"
         return self

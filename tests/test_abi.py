@@ -128,3 +128,20 @@ def test_block_sparse_builder_capacity(lib):
     qr = (ctypes.c_int32 * 3)()
     rc = lib.ulysses_bsmask_build_window_global(2048, 128, 4, 3, 16, rp, kc, cp, qr, ctypes.byref(n))
     assert rc == U.ERR_INVALID_ARG and n.value == 123
+
+
+def test_grouped_kv_head_counts_are_validated(lib):
+    """H_kv must divide H, and either H_kv % P == 0 or P % H_kv == 0; rejected before any launch."""
+    m = U.MaskStruct(U.MASK_CAUSAL, 128, None, None, None, None, 0)
+    p = [256 * (i + 1) for i in range(5)]
+    bad_group = U.Shape(1, 256, 8, 64, 4, 3)    # H % H_kv != 0
+    bad_cut = U.Shape(1, 256, 12, 64, 4, 6)     # neither H_kv % P nor P % H_kv is 0
+    for s in (bad_group, bad_cut):
+        assert U.ulysses_attn_bwd_workspace_size(s) == 0
+        assert U.ulysses_attn_fwd(s, m, 0.0, 0, *p, 0) == U.ERR_INVALID_ARG
+        assert U.ulysses_kv_seq_to_head(s, 256, 512, 0) == U.ERR_INVALID_ARG
+        assert U.ulysses_kv_head_to_seq_sum(s, 256, 512, 0) == U.ERR_INVALID_ARG
+    # accepted: whole key/value heads per group, and copies
+    for hkv in (8, 4, 2, 1):
+        assert U.ulysses_attn_bwd_workspace_size(U.Shape(1, 256, 8, 64, 4, hkv)) > 0
+    assert U.ulysses_kv_seq_to_head(U.Shape(0, 256, 8, 64, 4, 2), 0, 0, 0) == U.OK   # empty batch

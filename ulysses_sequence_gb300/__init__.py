@@ -25,8 +25,9 @@ MASK_NONE, MASK_CAUSAL, MASK_BLOCK_SPARSE = 0, 1, 2
 
 
 class Shape(ctypes.Structure):
+    """ulysses_shape_t; H_kv = 0 (the default) means H key/value heads."""
     _fields_ = [("B", ctypes.c_int), ("L", ctypes.c_int), ("H", ctypes.c_int), ("d_h", ctypes.c_int),
-                ("P", ctypes.c_int)]
+                ("P", ctypes.c_int), ("H_kv", ctypes.c_int)]
 
 
 class MaskStruct(ctypes.Structure):
@@ -35,7 +36,8 @@ class MaskStruct(ctypes.Structure):
                 ("nnz", ctypes.c_int)]
 
 
-EXPORTS = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_attn_fwd", "ulysses_attn_bwd_workspace_size",
+EXPORTS = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_kv_seq_to_head", "ulysses_kv_head_to_seq_sum",
+           "ulysses_attn_fwd", "ulysses_attn_bwd_workspace_size",
            "ulysses_attn_bwd", "ulysses_attn_bwd_noalloc", "ulysses_bsmask_build_window_global",
            "ulysses_get_device_status", "ulysses_selftest_timeout", "ulysses_status_string")
 BWD_NOALLOC_SCRATCH_BYTES = 96 * 1024 * 1024  # ULYSSES_BWD_NOALLOC_SCRATCH_BYTES
@@ -54,6 +56,8 @@ def load() -> ctypes.CDLL:
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.ulysses_seq_to_head.argtypes = [Shape, vp, vp, vp]
     lib.ulysses_head_to_seq.argtypes = [Shape, vp, vp, vp]
+    lib.ulysses_kv_seq_to_head.argtypes = [Shape, vp, vp, vp]
+    lib.ulysses_kv_head_to_seq_sum.argtypes = [Shape, vp, vp, vp]
     lib.ulysses_attn_fwd.argtypes = [Shape, ctypes.POINTER(MaskStruct), f, i, vp, vp, vp, vp, vp, vp]
     lib.ulysses_attn_bwd_workspace_size.argtypes = [Shape]
     lib.ulysses_attn_bwd_workspace_size.restype = sz
@@ -86,6 +90,14 @@ def ulysses_seq_to_head(shape: Shape, inp: int, out: int, stream: int) -> int:
 
 def ulysses_head_to_seq(shape: Shape, inp: int, out: int, stream: int) -> int:
     return load().ulysses_head_to_seq(shape, inp, out, stream)
+
+
+def ulysses_kv_seq_to_head(shape: Shape, inp: int, out: int, stream: int) -> int:
+    return load().ulysses_kv_seq_to_head(shape, inp, out, stream)
+
+
+def ulysses_kv_head_to_seq_sum(shape: Shape, inp: int, out: int, stream: int) -> int:
+    return load().ulysses_kv_head_to_seq_sum(shape, inp, out, stream)
 
 
 def ulysses_attn_fwd(shape: Shape, mask: MaskStruct, softmax_scale: float, io_layout: int, q: int, k: int, v: int,
@@ -233,15 +245,52 @@ def head_to_seq(y, P: int, out=None, stream=None):
     return out
 
 
-def _shape_of(x, P: int, layout: int) -> Shape:
-    return token_shape(x, P) if layout == LAYOUT_TOKEN_SHARDED else head_shape(x, P)
+def kv_heads_per_group(H_kv: int, P: int) -> int:
+    """Key/value heads each head group holds: H_kv / P, or 1 when P > H_kv (a copy)."""
+    return H_kv // P if H_kv % P == 0 else 1
+
+
+def kv_seq_to_head(x, P: int, out=None, stream=None):
+    """K/V [P][B][Lp][H_kv][d] -> [P][B][L][Hkvp][d] (heads replicated when P > H_kv)."""
+    import torch
+    Pn, B, Lp, Hkv, d = x.shape
+    if out is None:
+        out = torch.empty((P, B, Lp * P, kv_heads_per_group(Hkv, P), d), dtype=x.dtype, device=x.device)
+    shape = Shape(B, Lp * P, Hkv, d, P, Hkv)
+    check(ulysses_kv_seq_to_head(shape, x.data_ptr(), out.data_ptr(), _stream(stream)), "kv_seq_to_head")
+    return out
+
+
+def kv_head_to_seq_sum(y, P: int, H_kv: int, out=None, stream=None):
+    """Adjoint of kv_seq_to_head on bf16 gradients: [P][B][L][Hkvp][d] -> [P][B][Lp][H_kv][d],
+    the copies of each key/value head summed in fp32."""
+    import torch
+    Pn, B, L, Hkvp, d = y.shape
+    if out is None:
+        out = torch.empty((P, B, L // P, H_kv, d), dtype=y.dtype, device=y.device)
+    shape = Shape(B, L, H_kv, d, P, H_kv)
+    check(ulysses_kv_head_to_seq_sum(shape, y.data_ptr(), out.data_ptr(), _stream(stream)), "kv_head_to_seq_sum")
+    return out
+
+
+def _shape_of(x, P: int, layout: int, k=None, kv_heads: int = 0) -> Shape:
+    """Shape of query-side tensor x; H_kv from kv_heads, else from k's head dimension (in the
+    head layout k's Hkvp * P, which needs kv_heads when key/value heads are replicated)."""
+    s = token_shape(x, P) if layout == LAYOUT_TOKEN_SHARDED else head_shape(x, P)
+    if kv_heads:
+        s.H_kv = kv_heads
+    elif k is not None:
+        s.H_kv = k.shape[3] if layout == LAYOUT_TOKEN_SHARDED else k.shape[3] * P
+    return s
 
 
 def attn_fwd(q, k, v, P: int, mask: Mask, layout: int = LAYOUT_TOKEN_SHARDED, scale: float = 0.0, o=None,
-             lse=None, stream=None):
-    """Attention forward through ulysses_attn_fwd. Returns (o, lse[P][B][Hp][L] fp32)."""
+             lse=None, stream=None, kv_heads: int = 0):
+    """Attention forward through ulysses_attn_fwd. Returns (o, lse[P][B][Hp][L] fp32).
+    k, v may have fewer heads than q (grouped key/value heads; kv_heads names H_kv when the
+    head layout replicates them)."""
     import torch
-    shape = _shape_of(q, P, layout)
+    shape = _shape_of(q, P, layout, k, kv_heads)
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
@@ -258,10 +307,11 @@ def bwd_workspace(q, P: int, layout: int = LAYOUT_TOKEN_SHARDED):
 
 
 def attn_bwd(q, k, v, o, lse, do, P: int, mask: Mask, layout: int = LAYOUT_TOKEN_SHARDED, scale: float = 0.0,
-             dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """Attention backward through ulysses_attn_bwd. Returns (dq, dk, dv)."""
+             dq=None, dk=None, dv=None, workspace=None, stream=None, kv_heads: int = 0):
+    """Attention backward through ulysses_attn_bwd. Returns (dq, dk, dv); dk, dv are shaped
+    like k, v (with replicated key/value heads in the head layout: one part per copy)."""
     import torch
-    shape = _shape_of(q, P, layout)
+    shape = _shape_of(q, P, layout, k, kv_heads)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv

@@ -69,13 +69,14 @@ uint32_t* device_error_word() {
     return g_err[dev];
 }
 
-bool encode_qkv_map(CUtensorMap* map, const void* base, const ulysses_shape_t& s, int layout, int box_rows) {
+bool encode_qkv_map(CUtensorMap* map, const void* base, const ulysses_shape_t& s, int layout, int box_rows,
+                    int heads, int group_heads) {
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!load_encode_fn()) return false;
     }
-    const uint64_t d = s.d_h, H = s.H, P = s.P, B = s.B, L = s.L;
-    const uint64_t Hp = H / P, Lp = L / P;
+    const uint64_t d = s.d_h, H = heads, P = s.P, B = s.B, L = s.L;
+    const uint64_t Hp = group_heads, Lp = L / P;
     cuuint64_t dims[5];
     cuuint64_t strides[4];  // bytes, dims 1..4
     if (layout == ULYSSES_LAYOUT_TOKEN_SHARDED) {
@@ -98,8 +99,11 @@ bool encode_qkv_map(CUtensorMap* map, const void* base, const ulysses_shape_t& s
 namespace {
 
 int validate_shape(const ulysses_shape_t& s) {
-    if (s.B < 0 || s.L < 0 || s.H <= 0 || s.d_h <= 0 || s.P <= 0) return ULYSSES_ERR_INVALID_ARG;
+    if (s.B < 0 || s.L < 0 || s.H <= 0 || s.d_h <= 0 || s.P <= 0 || s.H_kv < 0) return ULYSSES_ERR_INVALID_ARG;
     if (s.H % s.P != 0 || s.L % s.P != 0) return ULYSSES_ERR_INVALID_ARG;
+    // grouped key/value heads: whole groups of query heads, and whole (or replicated) heads per group
+    const int hkv = shape_hkv(s);
+    if (s.H % hkv != 0 || (hkv % s.P != 0 && s.P % hkv != 0)) return ULYSSES_ERR_INVALID_ARG;
     // element counts must fit the kernels' 64-bit offsets and 32-bit row counters
     if (uint64_t(s.B) * uint64_t(s.L) * uint64_t(s.H) * uint64_t(s.d_h) > (1ull << 40)) return ULYSSES_ERR_INVALID_ARG;
     return ULYSSES_OK;
@@ -181,6 +185,36 @@ int ulysses_seq_to_head(ulysses_shape_t shape, const void* in, void* out, void* 
 
 int ulysses_head_to_seq(ulysses_shape_t shape, const void* in, void* out, void* stream) {
     return relayout_common(shape, in, out, stream, false);
+}
+
+// Key/value relayouts: without replication they are the plain relayouts of a tensor with
+// H_kv heads; with it (P > H_kv) a dedicated kernel copies (seq->head) or sums (head->seq).
+static int kv_relayout_common(ulysses_shape_t shape, const void* in, void* out, void* stream, bool to_head) {
+    // only B, L, d_h, P and the key/value head count take part (H only when H_kv is 0)
+    const int hkv = shape_hkv(shape);
+    if (shape.B < 0 || shape.L < 0 || shape.d_h <= 0 || shape.P <= 0 || hkv <= 0 || shape.L % shape.P != 0 ||
+        (hkv % shape.P != 0 && shape.P % hkv != 0))
+        return ULYSSES_ERR_INVALID_ARG;
+    if (uint64_t(shape.B) * uint64_t(shape.L) * uint64_t(hkv) * uint64_t(shape.d_h) > (1ull << 40))
+        return ULYSSES_ERR_INVALID_ARG;
+    const KvInfo kv = kv_info(shape);
+    if (uint64_t(shape.B) * shape.L * kv.Hkv * shape.d_h == 0) return ULYSSES_OK;
+    if (!in || !out) return ULYSSES_ERR_INVALID_ARG;
+    if (in == out) return ULYSSES_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 1u) return ULYSSES_ERR_MISALIGNED;
+    ulysses_shape_t s = shape;
+    s.H = kv.Hkv;
+    s.H_kv = kv.Hkv;
+    if (kv.rep == 1) return launch_relayout(s, in, out, static_cast<cudaStream_t>(stream), to_head);
+    return launch_kv_replicated(s, in, out, static_cast<cudaStream_t>(stream), to_head);
+}
+
+int ulysses_kv_seq_to_head(ulysses_shape_t shape, const void* in, void* out, void* stream) {
+    return kv_relayout_common(shape, in, out, stream, true);
+}
+
+int ulysses_kv_head_to_seq_sum(ulysses_shape_t shape, const void* in, void* out, void* stream) {
+    return kv_relayout_common(shape, in, out, stream, false);
 }
 
 int ulysses_attn_fwd(ulysses_shape_t shape, const ulysses_mask_t* mask, float softmax_scale, int io_layout,

@@ -35,6 +35,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdParams {
     int B, L, H, Hp, Lp, P;
+    int Hkv, G, Hkvp, kv_rep;  // key/value heads, query heads per key/value head, per group, copies
     int layout;
     int n_tiles;     // ceil(L / 128): key tiles and query steps
     int box_rows;    // TMA box rows (divides 128; boxes never straddle a shard)
@@ -105,6 +106,71 @@ __device__ __forceinline__ size_t row_offset(const BwdParams& p, int s, int h, i
     return ((size_t(g) * p.B + b) * p.L + s) * size_t(p.Hp) * D + size_t(j) * D;
 }
 
+// The key/value head a CTA of the backward owns (grid y = unit), and the query heads that
+// attend with it: h_first .. h_first + nqh - 1.
+struct KvUnit {
+    int b;
+    int kv;       // key/value head: in the token layout its index, in the head layout its index within group g
+    int g;        // head group (head layout)
+    int h_first;  // first query head
+    int nqh;      // query heads
+};
+
+__device__ __forceinline__ KvUnit kv_unit(const BwdParams& p, int unit) {
+    KvUnit u;
+    if (p.layout == ULYSSES_LAYOUT_TOKEN_SHARDED) {
+        u.b = unit / p.Hkv;
+        u.kv = unit % p.Hkv;
+        u.g = 0;
+        u.h_first = u.kv * p.G;
+        u.nqh = p.G;
+    } else {
+        u.g = unit / (p.B * p.Hkvp);
+        const int rem = unit % (p.B * p.Hkvp);
+        u.b = rem / p.Hkvp;
+        u.kv = rem % p.Hkvp;
+        // without copies the group's query heads split into Hkvp runs of G; with copies every
+        // query head of the group attends with the group's one key/value head
+        u.h_first = u.g * p.Hp + (p.kv_rep == 1 ? u.kv * p.G : 0);
+        u.nqh = p.kv_rep == 1 ? p.G : p.Hp;
+    }
+    return u;
+}
+
+// K/V coordinates of global row s for the unit's key/value head
+__device__ __forceinline__ void kv_coords(const BwdParams& p, int s, const KvUnit& u, int& c1, int& c2, int& c4) {
+    c1 = u.kv;
+    if (p.layout == ULYSSES_LAYOUT_TOKEN_SHARDED) {
+        c2 = s % p.Lp;
+        c4 = s / p.Lp;
+    } else {
+        c2 = s;
+        c4 = u.g;
+    }
+}
+
+// rows [s0, s0 + 128) of the unit's key/value head into D/64 swizzled chunks of 128 x 64
+template <int D>
+__device__ __forceinline__ void kv_load(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, const BwdParams& p,
+                                        int s0, const KvUnit& u) {
+    for (int c = 0; c < D / 64; ++c) {
+        for (int r = 0; r < kTile; r += p.box_rows) {
+            int c1, c2, c4;
+            kv_coords(p, s0 + r, u, c1, c2, c4);
+            tma_load_5d(dst + c * BwdCfg<D>::CHUNK + r * 128, map, bar, c * 64, c1, c2, u.b, c4);
+        }
+    }
+}
+
+// element offset of row s of the unit's key/value head in a K/V-shaped tensor
+__device__ __forceinline__ size_t kv_row_offset(const BwdParams& p, int s, const KvUnit& u, int D) {
+    if (p.layout == ULYSSES_LAYOUT_TOKEN_SHARDED) {
+        const int r = s / p.Lp, t = s % p.Lp;
+        return ((size_t(r) * p.B + u.b) * p.Lp + t) * size_t(p.Hkv) * D + size_t(u.kv) * D;
+    }
+    return ((size_t(u.g) * p.B + u.b) * p.L + s) * size_t(p.Hkvp) * D + size_t(u.kv) * D;
+}
+
 __device__ __forceinline__ size_t stat_index(const BwdParams& p, int s, int h, int b) {
     const int g = h / p.Hp, j = h % p.Hp;
     return ((size_t(g) * p.B + b) * p.Hp + j) * p.L + s;
@@ -169,12 +235,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int lane = static_cast<int>(lane_id());
     // key tiles vary fastest, so the CTAs resident at one time share one head and its
     // fp32 dQ accumulator stays in L2
-    const int bh = blockIdx.y;
-    const int b = bh / p.H;
-    const int h = bh % p.H;
+    const KvUnit u = kv_unit(p, blockIdx.y);
+    const int b = u.b;
     const int kt = blockIdx.x;
     int q_first = 0;
-    const int n_it = bwd_q_count<MASK>(p, kt, q_first);
+    const int n_per = bwd_q_count<MASK>(p, kt, q_first);  // query steps per query head
+    const int n_it = n_per * u.nqh;                        // steps over all the unit's query heads
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
@@ -215,8 +281,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tma_prefetch_desc(&tm_v);
                 tma_prefetch_desc(&tm_do);
                 mbar_arrive_expect_tx(kv_full, 2 * C::T_BYTES);
-                bwd_load<D>(sK, &tm_k, kv_full, p, kt * kTile, h, b);
-                bwd_load<D>(sV, &tm_v, kv_full, p, kt * kTile, h, b);
+                kv_load<D>(sK, &tm_k, kv_full, p, kt * kTile, u);
+                kv_load<D>(sV, &tm_v, kv_full, p, kt * kTile, u);
             }
             // lse and Delta arrive by bulk copy when the step is whole and 16-byte aligned
             const bool bulk_stats = (p.L % 4) == 0;
@@ -226,7 +292,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     ok = __all_sync(0xffffffffu, mbar_wait(q_empty + qs, ((it >> 1) - 1) & 1, ab, ROLE_LOAD, 1));
                     if (!ok) break;
                 }
-                const int q0 = bwd_q_step<MASK>(p, q_first, it) * kQStep;
+                const int ih = it / n_per;
+                const int h = u.h_first + ih;
+                const int q0 = bwd_q_step<MASK>(p, q_first, it - ih * n_per) * kQStep;
                 const bool whole = bulk_stats && q0 + kQStep <= p.L;
                 if (!whole) {
                     for (int c = lane; c < kQStep; c += 32) {
@@ -363,7 +431,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int key = kt * kTile + row;
         // this warp's chunk of the dS^T buffer (64 queries of every key)
         const uint32_t dst_chunk = smem_u32(sDSt) + hf * (C::DST_BYTES / 2);
-        float* acc_head = p.dq_acc + size_t(b * p.H + h) * p.n_tiles * kTile * D;
         const bool dq_lanes = wq * 32 < D;  // warp-uniform: d = 64 leaves quadrants 2, 3 without dQ rows
         bool ok = true;
         // Per step: dS of this step, then P of the next step (whose S^T the MMA issuer
@@ -373,7 +440,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // P = exp(scale S - lse) of step j over S^T, written back as bf16 P^T (A operand of dV)
         auto softmax_p = [&](int j) -> bool {
             const int qs = j & 1;
-            const int q0 = bwd_q_step<MASK>(p, q_first, j) * kQStep + 64 * hf;
+            const int jh = j / n_per;
+            const int q0 = bwd_q_step<MASK>(p, q_first, j - jh * n_per) * kQStep + 64 * hf;
             if (!__all_sync(0xffffffffu, mbar_wait(q_full + qs, (j >> 1) & 1, ab, ROLE_SOFTMAX, 1) &&
                                              mbar_wait(s_full, j & 1, ab, ROLE_SOFTMAX, 2)))
                 return false;
@@ -402,7 +470,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (n_it > 0) ok = softmax_p(0);
         for (int it = 0; ok && it < n_it; ++it) {
             const int qs = it & 1;
-            const int qstep = bwd_q_step<MASK>(p, q_first, it);
+            const int ih = it / n_per;
+            const int h = u.h_first + ih;
+            const int qstep = bwd_q_step<MASK>(p, q_first, it - ih * n_per);
             ok = __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, ab, ROLE_SOFTMAX, 3));
             if (!ok) break;
             tc_fence_after();
@@ -449,7 +519,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (dq_lanes) {
                 // one coalesced 128-byte reduction per query: the warp's 32 lanes are 32
                 // consecutive features of that query's row of the accumulator
-                float* dst = acc_head + size_t(qstep * kQStep + 64 * hf) * D + wq * 32 + lane;
+                float* dst = p.dq_acc + (size_t(b * p.H + h) * p.n_tiles * kTile + qstep * kQStep + 64 * hf) * D +
+                             wq * 32 + lane;
 #pragma unroll
                 for (int c = 0; c < 64; ++c) red_add_f32(dst + c * D, v[c]);
             }
@@ -461,7 +532,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // half 0 writes dV, half 1 writes dK
             const uint32_t tcol = hf == 0 ? C::T_DV : C::T_DK;
             const float mul = hf == 0 ? 1.0f : p.scale;
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(hf == 0 ? p.dv : p.dk) + row_offset(p, key, h, b, D);
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(hf == 0 ? p.dv : p.dk) + kv_row_offset(p, key, u, D);
             const bool valid = key < p.L;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -592,7 +663,9 @@ static int launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
             return ULYSSES_ERR_CUDA;
         attr_set[dev & 63] = true;
     }
-    dim3 grid(p.n_tiles, p.B * p.H);
+    // one CTA per (key tile, key/value head unit): B * Hkv units token-sharded, P * B * Hkvp head-sharded
+    const int units = p.layout == ULYSSES_LAYOUT_TOKEN_SHARDED ? p.B * p.Hkv : p.P * p.B * p.Hkvp;
+    dim3 grid(p.n_tiles, units);
     kern<<<grid, 320, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
     return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }
@@ -601,8 +674,10 @@ template <int D>
 static int launch_bwd_d(const ulysses_shape_t& s, const MaskArgs& m, BwdParams& p, const void* q, const void* k,
                         const void* v, const void* o, const void* dO, void* dq, cudaStream_t stream) {
     CUtensorMap mq, mk, mv, mdo;
-    if (!encode_qkv_map(&mq, q, s, p.layout, p.box_rows) || !encode_qkv_map(&mdo, dO, s, p.layout, p.box_rows) ||
-        !encode_qkv_map(&mk, k, s, p.layout, p.box_rows) || !encode_qkv_map(&mv, v, s, p.layout, p.box_rows))
+    if (!encode_qkv_map(&mq, q, s, p.layout, p.box_rows, s.H, s.H / s.P) ||
+        !encode_qkv_map(&mdo, dO, s, p.layout, p.box_rows, s.H, s.H / s.P) ||
+        !encode_qkv_map(&mk, k, s, p.layout, p.box_rows, p.Hkv, p.Hkvp) ||
+        !encode_qkv_map(&mv, v, s, p.layout, p.box_rows, p.Hkv, p.Hkvp))
         return ULYSSES_ERR_CUDA;
     const int sms = device_sm_count();
     const size_t rows = size_t(s.B) * s.H * s.L;
@@ -626,6 +701,8 @@ int launch_attn_bwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, in
                     void* dk, void* dv, void* workspace, cudaStream_t stream) {
     BwdParams p{};
     p.B = s.B; p.L = s.L; p.H = s.H; p.P = s.P; p.Hp = s.H / s.P; p.Lp = s.L / s.P;
+    const KvInfo kv = kv_info(s);
+    p.Hkv = kv.Hkv; p.G = kv.G; p.Hkvp = kv.Hkvp; p.kv_rep = kv.rep;
     p.layout = layout;
     p.n_tiles = (s.L + kTile - 1) / kTile;
     p.box_rows = layout == ULYSSES_LAYOUT_TOKEN_SHARDED ? gcd_int(p.Lp, kTile) : kTile;

@@ -35,6 +35,7 @@ namespace ulysses {
 
 struct FwdParams {
     int B, L, H, Hp, Lp, P;
+    int G, kv_rep;   // query heads per key/value head; head groups per key/value head copy
     int layout;      // 0 token-sharded, 1 head-sharded
     int n_tiles;     // ceil(L / 128)
     int n_pairs;     // ceil(n_tiles / 2)
@@ -62,27 +63,31 @@ struct FwdCfg {
     static constexpr uint32_t kThreads = 320;
 };
 
-// Coordinates of global row s of head h, batch b, in the 5-D map (d, head, row, batch, unit).
+// Coordinates of global row s of query head h, batch b, in the 5-D map (d, head, row,
+// batch, unit): of the query-side tensor, or (KV) of the key/value head that h attends with.
+template <bool KV>
 __device__ __forceinline__ void qkv_coords(const FwdParams& p, int s, int h, int& c1, int& c2, int& c4) {
     if (p.layout == ULYSSES_LAYOUT_TOKEN_SHARDED) {
-        c1 = h;
+        c1 = KV ? h / p.G : h;
         c2 = s % p.Lp;
         c4 = s / p.Lp;  // == P past the end of the sequence: out of bounds, filled with zeros
     } else {
-        c1 = h % p.Hp;
+        // head group g holds key/value heads [g Hkvp, (g + 1) Hkvp), or one copy of head g / kv_rep
+        c1 = KV ? (p.kv_rep == 1 ? (h % p.Hp) / p.G : 0) : h % p.Hp;
         c2 = s;
         c4 = h / p.Hp;
     }
 }
 
-// Loads rows [s0, s0 + 128) of head h into a tile of D/64 swizzled chunks of 128 x 64.
-template <int D>
+// Loads rows [s0, s0 + 128) of query head h (KV: of its key/value head) into a tile of D/64
+// swizzled chunks of 128 x 64.
+template <int D, bool KV>
 __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, const FwdParams& p,
                                           int s0, int h, int b) {
     for (int c = 0; c < D / 64; ++c) {
         for (int r = 0; r < kTile; r += p.box_rows) {
             int c1, c2, c4;
-            qkv_coords(p, s0 + r, h, c1, c2, c4);
+            qkv_coords<KV>(p, s0 + r, h, c1, c2, c4);
             tma_load_5d(dst + c * FwdCfg<D>::CHUNK_BYTES + r * 128, map, bar, c * 64, c1, c2, b, c4);
         }
     }
@@ -212,17 +217,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (!any) {
                     any = true;
                     mbar_arrive_expect_tx(q_full, 2 * C::TILE_BYTES);
-                    load_tile<D>(sQ, &tm_q, q_full, p, qt0 * kTile, h, b);
-                    load_tile<D>(sQ + C::TILE_BYTES, &tm_q, q_full, p, (qt0 + 1) * kTile, h, b);
+                    load_tile<D, false>(sQ, &tm_q, q_full, p, qt0 * kTile, h, b);
+                    load_tile<D, false>(sQ + C::TILE_BYTES, &tm_q, q_full, p, (qt0 + 1) * kTile, h, b);
                 }
                 const int sk = j % NSK, sv = j % NSV;
                 if (j >= NSK && !(ok = mbar_wait(k_empty + sk, ((j / NSK) - 1) & 1, ab, ROLE_LOAD, 1))) break;
                 mbar_arrive_expect_tx(k_full + sk, C::TILE_BYTES);
-                load_tile<D>(sK + sk * C::TILE_BYTES, &tm_k, k_full + sk, p, kt * kTile, h, b);
+                load_tile<D, true>(sK + sk * C::TILE_BYTES, &tm_k, k_full + sk, p, kt * kTile, h, b);
                 ++nk;
                 if (j >= NSV && !(ok = mbar_wait(v_empty + sv, ((j / NSV) - 1) & 1, ab, ROLE_LOAD, 2))) break;
                 mbar_arrive_expect_tx(v_full + sv, C::TILE_BYTES);
-                load_tile<D>(sV + sv * C::TILE_BYTES, &tm_v, v_full + sv, p, kt * kTile, h, b);
+                load_tile<D, true>(sV + sv * C::TILE_BYTES, &tm_v, v_full + sv, p, kt * kTile, h, b);
                 ++nv;
             }
             if (!ok) {
@@ -481,6 +486,9 @@ int launch_attn_fwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, in
                     const void* k, const void* v, void* o, float* lse, cudaStream_t stream) {
     FwdParams p{};
     p.B = s.B; p.L = s.L; p.H = s.H; p.P = s.P; p.Hp = s.H / s.P; p.Lp = s.L / s.P;
+    const KvInfo kv = kv_info(s);
+    p.G = kv.G;
+    p.kv_rep = kv.rep;
     p.layout = layout;
     p.n_tiles = (s.L + kTile - 1) / kTile;
     p.n_pairs = (p.n_tiles + 1) / 2;
@@ -493,8 +501,9 @@ int launch_attn_fwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, in
     p.err = device_error_word();
     if (!p.err) return ULYSSES_ERR_CUDA;
     CUtensorMap mq, mk, mv;
-    if (!encode_qkv_map(&mq, q, s, layout, p.box_rows) || !encode_qkv_map(&mk, k, s, layout, p.box_rows) ||
-        !encode_qkv_map(&mv, v, s, layout, p.box_rows))
+    if (!encode_qkv_map(&mq, q, s, layout, p.box_rows, s.H, s.H / s.P) ||
+        !encode_qkv_map(&mk, k, s, layout, p.box_rows, kv.Hkv, kv.Hkvp) ||
+        !encode_qkv_map(&mv, v, s, layout, p.box_rows, kv.Hkv, kv.Hkvp))
         return ULYSSES_ERR_CUDA;
     if (s.d_h == 128) {
         if (m.kind == ULYSSES_MASK_CAUSAL) return launch_fwd_t<128, ULYSSES_MASK_CAUSAL>(mq, mk, mv, p, stream);

@@ -8,6 +8,8 @@
 // out[((g*B + b)*L + r*Lp + t)*Hp*d]; head->seq moves it back. Runs are at least 256 bytes
 // at every workload size, so 16-byte vector loads and stores are coalesced on both sides
 // without staging: a warp copies whole token rows, with index arithmetic once per row.
+#include <type_traits>
+
 #include "common.cuh"
 #include "ulysses_internal.h"
 
@@ -146,6 +148,115 @@ int launch_relayout(const ulysses_shape_t& s, const void* in, void* out, cudaStr
         const uint64_t cap = uint64_t(sms) * 16;
         if (blocks > cap) blocks = cap;
         relayout_elem_kernel<<<unsigned(blocks), kThreads, 0, stream>>>(e, total);
+    }
+    return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------------------
+// Key/value relayouts with replicated heads (P > Hkv): head group g holds one key/value
+// head, g / rep with rep = P / Hkv (head-sharded [P][B][L][1][d]).
+//   seq->head: every destination row copies its source head's d elements;
+//   head->seq: every key/value head receives the fp32 sum of its rep copies (ascending g),
+//              rounded to bf16 (the adjoint, for gradients).
+// One thread per VEC consecutive elements of a destination row.
+// ---------------------------------------------------------------------------------------
+struct KvRepArgs {
+    const void* in;
+    void* out;
+    uint64_t P, B, L, Lp, Hkv, d, rep;
+};
+
+template <int VEC>
+__global__ void __launch_bounds__(256) kv_rep_to_head_kernel(KvRepArgs a, uint64_t total) {
+    using T = typename std::conditional<VEC == 8, uint4, uint16_t>::type;
+    const T* in = static_cast<const T*>(a.in);
+    T* out = static_cast<T*>(a.out);
+    const uint64_t dv = a.d / VEC;
+    for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += uint64_t(gridDim.x) * blockDim.x) {
+        // destination [g][b][s][v]
+        const uint64_t v = i % dv;
+        const uint64_t row = i / dv;
+        const uint64_t s = row % a.L;
+        const uint64_t gb = row / a.L;
+        const uint64_t b = gb % a.B;
+        const uint64_t g = gb / a.B;
+        const uint64_t h = g / a.rep;
+        const uint64_t src = (((s / a.Lp) * a.B + b) * a.Lp + s % a.Lp) * a.Hkv + h;
+        out[i] = in[src * dv + v];
+    }
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(256) kv_rep_to_seq_sum_kernel(KvRepArgs a, uint64_t total) {
+    const __nv_bfloat16* in = static_cast<const __nv_bfloat16*>(a.in);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    const uint64_t dv = a.d / VEC;
+    for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += uint64_t(gridDim.x) * blockDim.x) {
+        // destination [r][b][t][h][v]
+        const uint64_t v = i % dv;
+        const uint64_t row = i / dv;
+        const uint64_t h = row % a.Hkv;
+        const uint64_t tok = row / a.Hkv;  // (r * B + b) * Lp + t
+        const uint64_t t = tok % a.Lp;
+        const uint64_t rb = tok / a.Lp;
+        const uint64_t b = rb % a.B;
+        const uint64_t r = rb / a.B;
+        const uint64_t s = r * a.Lp + t;
+        float acc[VEC];
+#pragma unroll
+        for (int x = 0; x < VEC; ++x) acc[x] = 0.f;
+        for (uint64_t g = h * a.rep; g < (h + 1) * a.rep; ++g) {
+            const __nv_bfloat16* src = in + ((g * a.B + b) * a.L + s) * a.d + v * VEC;
+            if (VEC == 8) {
+                const uint4 w = *reinterpret_cast<const uint4*>(src);
+                const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+                for (int x = 0; x < VEC / 2; ++x) {
+                    const float2 f = __bfloat1622float2(w2[x]);
+                    acc[2 * x] += f.x;
+                    acc[2 * x + 1] += f.y;
+                }
+            } else {
+#pragma unroll
+                for (int x = 0; x < VEC; ++x) acc[x] += __bfloat162float(src[x]);
+            }
+        }
+        __nv_bfloat16* dst = out + i * VEC;
+        if (VEC == 8) {
+            uint4 w;
+            w.x = pack_bf16(acc[0], acc[1]);
+            w.y = pack_bf16(acc[2], acc[3]);
+            w.z = pack_bf16(acc[4], acc[5]);
+            w.w = pack_bf16(acc[6], acc[7]);
+            *reinterpret_cast<uint4*>(dst) = w;
+        } else {
+#pragma unroll
+            for (int x = 0; x < VEC; ++x) dst[x] = __float2bfloat16_rn(acc[x]);
+        }
+    }
+}
+
+int launch_kv_replicated(const ulysses_shape_t& s, const void* in, void* out, cudaStream_t stream, bool to_head) {
+    KvRepArgs a{};
+    a.in = in;
+    a.out = out;
+    a.P = uint64_t(s.P); a.B = uint64_t(s.B); a.L = uint64_t(s.L); a.Lp = a.L / a.P;
+    a.Hkv = uint64_t(s.H_kv); a.d = uint64_t(s.d_h); a.rep = a.P / a.Hkv;
+    const bool vec = (a.d % 8 == 0) && ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) % 16 == 0);
+    const uint64_t elems = to_head ? a.P * a.B * a.L * a.d : a.P * a.B * a.Lp * a.Hkv * a.d;
+    const uint64_t total = elems / (vec ? 8 : 1);
+    if (total == 0) return ULYSSES_OK;
+    uint64_t blocks = (total + 255) / 256;
+    const uint64_t cap = uint64_t(device_sm_count()) * 16;
+    if (blocks > cap) blocks = cap;
+    if (to_head) {
+        if (vec) kv_rep_to_head_kernel<8><<<unsigned(blocks), 256, 0, stream>>>(a, total);
+        else kv_rep_to_head_kernel<1><<<unsigned(blocks), 256, 0, stream>>>(a, total);
+    } else {
+        if (vec) kv_rep_to_seq_sum_kernel<8><<<unsigned(blocks), 256, 0, stream>>>(a, total);
+        else kv_rep_to_seq_sum_kernel<1><<<unsigned(blocks), 256, 0, stream>>>(a, total);
     }
     return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }

@@ -15,10 +15,29 @@ constexpr int kBwdQTile = 64;   // query rows per step of the backward kernel
 int device_sm_count();
 uint32_t* device_error_word();  // device address of this device's error word (nullptr on failure)
 
+// Key/value head arrangement of a shape (grouped-query attention when Hkv < H).
+struct KvInfo {
+    int Hkv;   // key/value heads
+    int G;     // query heads per key/value head, H / Hkv
+    int Hkvp;  // key/value heads per head group in the head-sharded layout
+    int rep;   // head groups holding a copy of each key/value head (1 unless P > Hkv)
+};
+inline int shape_hkv(const ulysses_shape_t& s) { return s.H_kv > 0 ? s.H_kv : s.H; }
+inline KvInfo kv_info(const ulysses_shape_t& s) {
+    KvInfo k{};
+    k.Hkv = shape_hkv(s);
+    k.G = s.H / k.Hkv;
+    if (k.Hkv % s.P == 0) { k.Hkvp = k.Hkv / s.P; k.rep = 1; }
+    else { k.Hkvp = 1; k.rep = s.P / k.Hkv; }
+    return k;
+}
+
 // Encodes a 5-D bf16 tensor map over (d, head, row, batch, unit) with a box of
-// (64, 1, box_rows, 1, 1), 128-byte swizzle and zero fill out of bounds.
-//   token layout: dims (d, H, Lp, B, P);  head layout: dims (d, Hp, L, B, P).
-bool encode_qkv_map(CUtensorMap* map, const void* base, const ulysses_shape_t& s, int layout, int box_rows);
+// (64, 1, box_rows, 1, 1), 128-byte swizzle and zero fill out of bounds, for a tensor with
+// `heads` heads in the token layout and `group_heads` per head group in the head layout:
+//   token layout: dims (d, heads, Lp, B, P);  head layout: dims (d, group_heads, L, B, P).
+bool encode_qkv_map(CUtensorMap* map, const void* base, const ulysses_shape_t& s, int layout, int box_rows,
+                    int heads, int group_heads);
 
 struct MaskArgs {
     int kind;
@@ -29,6 +48,8 @@ struct MaskArgs {
 };
 
 int launch_relayout(const ulysses_shape_t& s, const void* in, void* out, cudaStream_t stream, bool to_head);
+// Key/value relayouts with replication (P > Hkv): seq->head copies, head->seq sums the copies.
+int launch_kv_replicated(const ulysses_shape_t& s, const void* in, void* out, cudaStream_t stream, bool to_head);
 
 int launch_attn_fwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, int layout, const void* q,
                     const void* k, const void* v, void* o, float* lse, cudaStream_t stream);

@@ -47,6 +47,7 @@ class Workload:
     window_after: int = 3
     global_stride: int = 16
     sampled_rows: int = 0  # 0: the oracle checks every row
+    H_kv: int = 0          # key/value heads (grouped-query attention); 0: H
 
     @property
     def Lp(self) -> int:
@@ -55,6 +56,10 @@ class Workload:
     @property
     def Hp(self) -> int:
         return self.H // self.P
+
+    @property
+    def Hkv(self) -> int:
+        return self.H_kv or self.H
 
 
 WORKLOADS: Dict[str, Workload] = {
@@ -73,6 +78,10 @@ WORKLOADS: Dict[str, Workload] = {
         # an 8-tile sliding window plus every 16th key tile as global.
         Workload("block_sparse", 2, 65536, 32, 128, 8, "block_sparse", True, 4,
                  sampled_rows=4096),
+        # Grouped-query variant of the GPT-7B-like layer: 32 query heads share 8 key/value
+        # heads (groups of 4); each of the P=8 head groups receives one whole key/value head.
+        Workload("gpt7b_gqa", 1, 32768, 32, 128, 8, "causal", True, 5,
+                 q_scale=1.0 / math.sqrt(128.0), sampled_rows=4096, H_kv=8),
     ]
 }
 
@@ -91,17 +100,18 @@ def shard_tokens(x: torch.Tensor, P: int) -> torch.Tensor:
 
 
 def draw(B: int, L: int, H: int, d: int, P: int, seed: int, names: Iterable[str] = ("q", "k", "v", "do"),
-         q_scale: float = 1.0) -> Dict[str, torch.Tensor]:
+         q_scale: float = 1.0, H_kv: int = 0) -> Dict[str, torch.Tensor]:
     """Draw bf16 tensors in the token-sharded layout [P][B][L/P][H][d] from one CPU generator.
 
     Tensors are drawn in the order given (q, k, v, do by default) as fp32 N(0, 1) of the
-    logical shape [B, L, H, d]; q is multiplied by q_scale in fp32 before the
-    round-to-nearest-even conversion to bf16.
+    logical shape [B, L, H, d] (k and v with H_kv heads when H_kv is given); q is
+    multiplied by q_scale in fp32 before the round-to-nearest-even conversion to bf16.
     """
     g = torch.Generator().manual_seed(seed)
     out = {}
     for n in names:
-        x = torch.randn((B, L, H, d), generator=g, dtype=torch.float32)
+        heads = H_kv if (H_kv and n in ("k", "v")) else H
+        x = torch.randn((B, L, heads, d), generator=g, dtype=torch.float32)
         if n == "q" and q_scale != 1.0:
             x.mul_(q_scale)
         out[n] = shard_tokens(x.to(torch.bfloat16), P)
@@ -110,7 +120,7 @@ def draw(B: int, L: int, H: int, d: int, P: int, seed: int, names: Iterable[str]
 
 
 def draw_workload(w: Workload, names: Iterable[str] = ("q", "k", "v", "do")) -> Dict[str, torch.Tensor]:
-    return draw(w.B, w.L, w.H, w.d, w.P, w.seed, names, q_scale=w.q_scale)
+    return draw(w.B, w.L, w.H, w.d, w.P, w.seed, names, q_scale=w.q_scale, H_kv=w.H_kv)
 
 
 def sample_rows(B: int, L: int, n: int, seed: int) -> np.ndarray:
