@@ -449,13 +449,21 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_ld32(tmem + C::T_S + lane_off + 64 * hf, pv);
             tmem_ld32(tmem + C::T_S + lane_off + 64 * hf + 32, pv + 32);
             tmem_wait_ld();
-            const float* lse = sLSE + qs * kQStep + 64 * hf;
+            // every lane needs the same 64 lse values: 16-byte broadcast loads (a quarter of
+            // the shared-memory wavefronts of scalar ones, which compete with the MMA operands)
+            const float4* lse4 = reinterpret_cast<const float4*>(sLSE + qs * kQStep + 64 * hf);
             const bool diag = (MASK == ULYSSES_MASK_CAUSAL) && (q0 < key);
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                float e = ex2(fmaf(pv[c], p.scale_log2, -lse[c] * kLog2e));
-                if (diag && q0 + c < key) e = 0.f;
-                pv[c] = e;
+            for (int c4 = 0; c4 < 16; ++c4) {
+                const float4 l = lse4[c4];
+                const float nl[4] = {-l.x * kLog2e, -l.y * kLog2e, -l.z * kLog2e, -l.w * kLog2e};
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const int c = 4 * c4 + x;
+                    float e = ex2(fmaf(pv[c], p.scale_log2, nl[x]));
+                    if (diag && q0 + c < key) e = 0.f;
+                    pv[c] = e;
+                }
             }
             uint32_t pk[32];
 #pragma unroll
@@ -482,9 +490,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 float dp[32];
                 tmem_ld32(tmem + C::T_DP + lane_off + 64 * hf + 32 * hh, dp);
                 tmem_wait_ld();
-                const float* dl = sDelta + qs * kQStep + 64 * hf + 32 * hh;
+                const float4* dl4 = reinterpret_cast<const float4*>(sDelta + qs * kQStep + 64 * hf + 32 * hh);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) pv[32 * hh + c] = pv[32 * hh + c] * (dp[c] - dl[c]);
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const float4 dl = dl4[c4];
+                    const float dv4[4] = {dl.x, dl.y, dl.z, dl.w};
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const int c = 32 * hh + 4 * c4 + x;
+                        pv[c] = pv[c] * (dp[4 * c4 + x] - dv4[x]);
+                    }
+                }
             }
             {
                 uint32_t pk[32];
