@@ -22,6 +22,14 @@ What it computes, and where the pages define it:
   Matrix products use numpy's fp64 matmul as a library step; rows are independent, so
   the sampled mode evaluates the same formulas on a subset of rows.
 
+* ``qkv_projection`` / ``out_projection`` -- the steps on either side of the path: each
+  rank projects its own token shard to Q, K, V before the first all-to-all, and projects
+  the returned O after the second (paper summary section 3.2, "Big-Picture Architecture",
+  and section 3.4.1, "Before attention"; pinyu.ai page, "One attention block, end to
+  end"). Row r of a token shard is projected alone, so the projections are row-wise
+  products with the weight matrices (y = x W^T, numpy's fp64 matmul as a library step)
+  and keep the token-sharded layout.
+
 Readings where the pages are silent (each listed in the design doc): masked positions are
 excluded (-inf), a row with no permitted key has O = 0, LSE = -inf and zero gradients;
 the log-sum-exp is natural-log of the scaled scores, stored [P][B][H/P][L].
@@ -307,6 +315,37 @@ def attention_full(q_tok: np.ndarray, k_tok: np.ndarray, v_tok: np.ndarray, P: i
         out["dk"] = kv_head_to_seq_sum(grads["dk"], P, Hkv)
         out["dv"] = kv_head_to_seq_sum(grads["dv"], P, Hkv)
     return out
+
+
+# --------------------------------------------------------------------------- projections
+
+def _as_f64(x: np.ndarray) -> np.ndarray:
+    return bf16_to_f64(x) if x.dtype == np.uint16 else x.astype(np.float64)
+
+
+def qkv_projection(x_tok: np.ndarray, w_qkv: np.ndarray, H: int, Hkv: int, d: int) -> Dict[str, np.ndarray]:
+    """Local QKV projection of token-sharded hidden states.
+
+    x_tok [P][B][Lp][hidden] (bf16 bits or floats); w_qkv [(H + 2 Hkv) d][hidden], rows
+    ordered Q heads, then K heads, then V heads (y = x W^T). Returns fp64 "q"
+    [P][B][Lp][H][d], "k" and "v" [P][B][Lp][Hkv][d]: every token row of every shard is
+    projected on its own, so the outputs keep the token-sharded layout.
+    """
+    x = _as_f64(x_tok)
+    w = _as_f64(w_qkv)
+    P, B, Lp, hidden = x.shape
+    assert w.shape == ((H + 2 * Hkv) * d, hidden)
+    y = (x.reshape(-1, hidden) @ w.T).reshape(P, B, Lp, H + 2 * Hkv, d)
+    return {"q": y[:, :, :, :H], "k": y[:, :, :, H:H + Hkv], "v": y[:, :, :, H + Hkv:]}
+
+
+def out_projection(o_tok: np.ndarray, w_o: np.ndarray) -> np.ndarray:
+    """Output projection of the token-sharded attention output: o_tok [P][B][Lp][H][d],
+    w_o [hidden][H d]; returns fp64 [P][B][Lp][hidden] (y = o W_o^T per token row)."""
+    o = _as_f64(o_tok)
+    w = _as_f64(w_o)
+    P, B, Lp, H, d = o.shape
+    return (o.reshape(-1, H * d) @ w.T).reshape(P, B, Lp, w.shape[0])
 
 
 def _sampled_task(task):

@@ -393,3 +393,56 @@ def test_gqa_matches_torch_sdpa(P, H, Hkv):
     np.testing.assert_allclose(logical(g["o"]), o.detach().permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-12)
     for name, t in (("dq", tq), ("dk", tk), ("dv", tv)):
         np.testing.assert_allclose(logical(g[name]), t.grad.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-11)
+
+
+# --------------------------------------------------------------------------- projections
+
+def _perm_weight(n_out, n_in, seed):
+    """A 0/1 matrix whose row i selects input feature perm[i] (so y[:, i] = x[:, perm[i]])."""
+    perm = np.random.default_rng(seed).integers(0, n_in, size=n_out)
+    w = np.zeros((n_out, n_in))
+    w[np.arange(n_out), perm] = 1.0
+    return w, perm
+
+
+@pytest.mark.parametrize("P,H,Hkv,d", [(2, 4, 4, 8), (4, 8, 2, 16), (2, 4, 1, 8)])
+def test_qkv_projection_with_selection_weights(P, H, Hkv, d):
+    """One-hot weight rows copy chosen input features: catches a transposed weight, a wrong
+    Q/K/V block order and a wrong head split exactly."""
+    B, L, hidden = 2, 16, 24
+    x = RNG.standard_normal((P, B, L // P, hidden))
+    w, perm = _perm_weight((H + 2 * Hkv) * d, hidden, seed=H + Hkv)
+    out = oracle.qkv_projection(x, w, H, Hkv, d)
+    flat = x[..., perm]  # [P][B][Lp][(H + 2 Hkv) d]
+    np.testing.assert_array_equal(out["q"].reshape(P, B, L // P, -1), flat[..., :H * d])
+    np.testing.assert_array_equal(out["k"].reshape(P, B, L // P, -1), flat[..., H * d:(H + Hkv) * d])
+    np.testing.assert_array_equal(out["v"].reshape(P, B, L // P, -1), flat[..., (H + Hkv) * d:])
+
+
+def test_projections_match_torch_linear():
+    P, B, L, H, Hkv, d, hidden = 4, 2, 32, 4, 2, 8, 40
+    x = RNG.standard_normal((P, B, L // P, hidden))
+    w = RNG.standard_normal(((H + 2 * Hkv) * d, hidden))
+    wo = RNG.standard_normal((hidden, H * d))
+    out = oracle.qkv_projection(x, w, H, Hkv, d)
+    ref = torch.nn.functional.linear(torch.from_numpy(x), torch.from_numpy(w)).numpy()
+    got = np.concatenate([out[n].reshape(P, B, L // P, -1) for n in ("q", "k", "v")], axis=-1)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+    o = RNG.standard_normal((P, B, L // P, H, d))
+    y = oracle.out_projection(o, wo)
+    ref = torch.nn.functional.linear(torch.from_numpy(o.reshape(P, B, L // P, H * d)), torch.from_numpy(wo)).numpy()
+    np.testing.assert_allclose(y, ref, rtol=0, atol=1e-12)
+
+
+def test_projection_of_shards_equals_projection_of_the_sequence():
+    """Each rank projects its own tokens: sharding the sequence first or after gives the same rows."""
+    B, L, hidden, H, d = 2, 24, 16, 4, 8
+    x = RNG.standard_normal((B, L, hidden))
+    w = RNG.standard_normal((3 * H * d, hidden))
+    ref = oracle.qkv_projection(x[None], w, H, H, d)  # one shard holding the whole sequence
+    for P in (2, 3, 4):
+        x_tok = x.reshape(B, P, L // P, hidden).transpose(1, 0, 2, 3)
+        out = oracle.qkv_projection(x_tok, w, H, H, d)
+        for n in ("q", "k", "v"):
+            merged = out[n].transpose(1, 0, 2, 3, 4).reshape(B, L, H, d)
+            np.testing.assert_allclose(merged, ref[n][0], rtol=0, atol=1e-12)
