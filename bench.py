@@ -369,6 +369,26 @@ def main():
     rl_bytes = 2 * x["q"].numel() * x["q"].element_size()
     peak_tf, peak_gbs, peak_src = measured_peaks()
 
+    # ---- the projections on either side of the block (hidden = H d_h): QKV into the
+    # token-sharded layout the attention reads, and the output projection of O
+    hidden = w.H * w.d
+    xs = workloads.draw_hidden(w.B, w.L, hidden, w.P, seed=w.seed + 7).to(dev)
+    w_qkv = workloads.draw_weight((w.H + 2 * w.Hkv) * w.d, hidden, seed=w.seed + 8).to(dev)
+    w_o = workloads.draw_weight(hidden, w.H * w.d, seed=w.seed + 9).to(dev)
+    pq, pk, pv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
+    py = torch.empty_like(xs)
+    qkv_call = lambda: U.qkv_proj(xs, w_qkv, w.P, w.H, w.Hkv, w.d, q=pq, k=pk, v=pv)  # noqa: E731
+    out_call = lambda: U.out_proj(o, w_o, w.P, y=py)  # noqa: E731
+    for _ in range(3):
+        qkv_call()
+        out_call()
+    qkv_ms = cuda_events_time(qkv_call, stream, 10)
+    out_ms = cuda_events_time(out_call, stream, 10)
+    rows = w.B * w.L
+    qkv_flops = 2 * rows * (w.H + 2 * w.Hkv) * w.d * hidden
+    out_flops = 2 * rows * hidden * w.H * w.d
+    del xs, w_qkv, w_o, pq, pk, pv, py
+
     # ---- dominant launch group: the backward call (Delta prep + main + dQ convert)
     bwd_avg = statistics.mean(bwd_ms) if w.backward else 0.0
     fwd_avg = statistics.mean(fwd_ms)
@@ -420,6 +440,11 @@ def main():
             "permitted_pairs_per_head": pairs,
             "relayout": {"kernel": "seq_to_head (one tensor)", "gbs": rl_bytes / (rl_ms * 1e-3) / 1e9,
                          "ms": rl_ms, "bytes": rl_bytes, "frac_of_measured_hbm": rl_bytes / (rl_ms * 1e-3) / 1e9 / peak_gbs},
+            "projections": {"qkv_tflops": qkv_flops / (qkv_ms * 1e-3) / 1e12, "qkv_ms": qkv_ms,
+                            "out_tflops": out_flops / (out_ms * 1e-3) / 1e12, "out_ms": out_ms,
+                            "qkv_frac": qkv_flops / (qkv_ms * 1e-3) / 1e12 / peak_tf,
+                            "out_frac": out_flops / (out_ms * 1e-3) / 1e12 / peak_tf,
+                            "note": "x [B*L][H*d_h] -> Q, K, V token-sharded; O -> y; not part of the step"},
             "accounted_alltoall_bytes_per_rank": {"fwd": comm, "leaves_rank": comm * (w.P - 1) // w.P,
                                                   "note": "4Nh/P in bf16 bytes, accounted, not measured over a link"},
             "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak_tf,

@@ -197,6 +197,24 @@ int ulysses_attn_bwd_noalloc(ulysses_shape_t shape, const ulysses_mask_t *mask, 
                              const void *o, const float *lse, const void *dO,
                              void *dq, void *dk, void *dv, void *stream);
 
+/* The projections on either side of the attention block (paper summary section 3.2
+ * "Big-Picture Architecture" and section 3.4.1 "Before attention"; pinyu.ai page "One
+ * attention block, end to end"): every rank projects its own token shard, so over the
+ * token-sharded layout both are matrix products over the M = B * L token rows
+ * [P][B][Lp], y = x W^T, bf16 in and out with fp32 accumulation.
+ *
+ * QKV projection: x [P][B][Lp][hidden]; w_qkv [(H + 2 H_kv) d_h][hidden], rows ordered
+ * Q heads, K heads, V heads. Writes q [P][B][Lp][H][d_h], k and v [P][B][Lp][H_kv][d_h],
+ * the token-sharded layout ulysses_attn_fwd reads (no relayout in between).
+ * Requires hidden, H d_h and H_kv d_h multiples of 32 (else ULYSSES_ERR_UNSUPPORTED);
+ * pointers 16-byte aligned. */
+int ulysses_qkv_proj(ulysses_shape_t shape, int hidden, const void *x, const void *w_qkv, void *q, void *k,
+                     void *v, void *stream);
+
+/* Output projection: o [P][B][Lp][H][d_h] (as ulysses_attn_fwd returns it, token-sharded);
+ * w_o [hidden][H d_h]; writes y [P][B][Lp][hidden]. Same requirements. */
+int ulysses_out_proj(ulysses_shape_t shape, int hidden, const void *o, const void *w_o, void *y, void *stream);
+
 /* Host helper: the block-sparse pattern "sliding window plus strided global key tiles".
  * Query tile qt gets key tiles max(0, qt - window_before) .. min(n - 1, qt + window_after)
  * and every kt with kt % global_stride == 0 (global_stride <= 0: none), n = ceil(L/tile).

@@ -37,7 +37,7 @@ class MaskStruct(ctypes.Structure):
 
 
 EXPORTS = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_kv_seq_to_head", "ulysses_kv_head_to_seq_sum",
-           "ulysses_attn_fwd", "ulysses_attn_bwd_workspace_size",
+           "ulysses_qkv_proj", "ulysses_out_proj", "ulysses_attn_fwd", "ulysses_attn_bwd_workspace_size",
            "ulysses_attn_bwd", "ulysses_attn_bwd_noalloc", "ulysses_bsmask_build_window_global",
            "ulysses_get_device_status", "ulysses_selftest_timeout", "ulysses_status_string")
 BWD_NOALLOC_SCRATCH_BYTES = 96 * 1024 * 1024  # ULYSSES_BWD_NOALLOC_SCRATCH_BYTES
@@ -57,6 +57,8 @@ def load() -> ctypes.CDLL:
     lib.ulysses_seq_to_head.argtypes = [Shape, vp, vp, vp]
     lib.ulysses_head_to_seq.argtypes = [Shape, vp, vp, vp]
     lib.ulysses_kv_seq_to_head.argtypes = [Shape, vp, vp, vp]
+    lib.ulysses_qkv_proj.argtypes = [Shape, i, vp, vp, vp, vp, vp, vp]
+    lib.ulysses_out_proj.argtypes = [Shape, i, vp, vp, vp, vp]
     lib.ulysses_kv_head_to_seq_sum.argtypes = [Shape, vp, vp, vp]
     lib.ulysses_attn_fwd.argtypes = [Shape, ctypes.POINTER(MaskStruct), f, i, vp, vp, vp, vp, vp, vp]
     lib.ulysses_attn_bwd_workspace_size.argtypes = [Shape]
@@ -98,6 +100,14 @@ def ulysses_kv_seq_to_head(shape: Shape, inp: int, out: int, stream: int) -> int
 
 def ulysses_kv_head_to_seq_sum(shape: Shape, inp: int, out: int, stream: int) -> int:
     return load().ulysses_kv_head_to_seq_sum(shape, inp, out, stream)
+
+
+def ulysses_qkv_proj(shape: Shape, hidden: int, x: int, w_qkv: int, q: int, k: int, v: int, stream: int) -> int:
+    return load().ulysses_qkv_proj(shape, hidden, x, w_qkv, q, k, v, stream)
+
+
+def ulysses_out_proj(shape: Shape, hidden: int, o: int, w_o: int, y: int, stream: int) -> int:
+    return load().ulysses_out_proj(shape, hidden, o, w_o, y, stream)
 
 
 def ulysses_attn_fwd(shape: Shape, mask: MaskStruct, softmax_scale: float, io_layout: int, q: int, k: int, v: int,
@@ -282,6 +292,31 @@ def _shape_of(x, P: int, layout: int, k=None, kv_heads: int = 0) -> Shape:
     elif k is not None:
         s.H_kv = k.shape[3] if layout == LAYOUT_TOKEN_SHARDED else k.shape[3] * P
     return s
+
+
+def qkv_proj(x, w_qkv, P: int, H: int, H_kv: int, d: int, q=None, k=None, v=None, stream=None):
+    """QKV projection of token-sharded hidden states x [P][B][Lp][hidden] with w_qkv
+    [(H + 2 H_kv) d][hidden]; returns q [P][B][Lp][H][d], k, v [P][B][Lp][H_kv][d]."""
+    import torch
+    Pn, B, Lp, hidden = x.shape
+    shape = Shape(B, Lp * P, H, d, P, H_kv)
+    q = torch.empty((P, B, Lp, H, d), dtype=x.dtype, device=x.device) if q is None else q
+    k = torch.empty((P, B, Lp, H_kv, d), dtype=x.dtype, device=x.device) if k is None else k
+    v = torch.empty((P, B, Lp, H_kv, d), dtype=x.dtype, device=x.device) if v is None else v
+    check(ulysses_qkv_proj(shape, hidden, x.data_ptr(), w_qkv.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                           _stream(stream)), "qkv_proj")
+    return q, k, v
+
+
+def out_proj(o, w_o, P: int, y=None, stream=None):
+    """Output projection of token-sharded o [P][B][Lp][H][d] with w_o [hidden][H d]."""
+    import torch
+    Pn, B, Lp, H, d = o.shape
+    hidden = w_o.shape[0]
+    y = torch.empty((P, B, Lp, hidden), dtype=o.dtype, device=o.device) if y is None else y
+    check(ulysses_out_proj(Shape(B, Lp * P, H, d, P), hidden, o.data_ptr(), w_o.data_ptr(), y.data_ptr(),
+                           _stream(stream)), "out_proj")
+    return y
 
 
 def attn_fwd(q, k, v, P: int, mask: Mask, layout: int = LAYOUT_TOKEN_SHARDED, scale: float = 0.0, o=None,

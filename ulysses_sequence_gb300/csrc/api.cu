@@ -69,6 +69,18 @@ uint32_t* device_error_word() {
     return g_err[dev];
 }
 
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
+                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                       const cuuint32_t* elem_strides) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!load_encode_fn()) return false;
+    }
+    return g_encode(map, dtype, rank, const_cast<void*>(base), dims, strides, box, elem_strides,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_qkv_map(CUtensorMap* map, const void* base, const ulysses_shape_t& s, int layout, int box_rows,
                     int heads, int group_heads) {
     {
@@ -215,6 +227,55 @@ int ulysses_kv_seq_to_head(ulysses_shape_t shape, const void* in, void* out, voi
 
 int ulysses_kv_head_to_seq_sum(ulysses_shape_t shape, const void* in, void* out, void* stream) {
     return kv_relayout_common(shape, in, out, stream, false);
+}
+
+// Projections: C[M][N] = A[M][K] B[N][K]^T over the M = B * L token rows of the token-sharded
+// layout. TMA needs 16-byte row pitches (K % 8 == 0); the epilogue routes 32-column chunks.
+static int validate_proj(const ulysses_shape_t& s, int hidden) {
+    int rc = validate_shape(s);
+    if (rc != ULYSSES_OK) return rc;
+    if (hidden <= 0) return ULYSSES_ERR_INVALID_ARG;
+    if (hidden % 32 != 0 || (s.H * s.d_h) % 32 != 0 || (shape_hkv(s) * s.d_h) % 32 != 0) return ULYSSES_ERR_UNSUPPORTED;
+    if (uint64_t(s.B) * s.L > 0x7fffffffull) return ULYSSES_ERR_UNSUPPORTED;
+    return ULYSSES_OK;
+}
+
+int ulysses_qkv_proj(ulysses_shape_t shape, int hidden, const void* x, const void* w_qkv, void* q, void* k, void* v,
+                     void* stream) {
+    int rc = validate_proj(shape, hidden);
+    if (rc != ULYSSES_OK) return rc;
+    const int M = shape.B * shape.L;
+    if (M == 0) return ULYSSES_OK;
+    if (!x || !w_qkv || !q || !k || !v) return ULYSSES_ERR_INVALID_ARG;
+    const void* ins[] = {x, w_qkv};
+    const void* outs[] = {q, k, v};
+    for (const void* a : outs)
+        for (const void* b : ins)
+            if (a == b) return ULYSSES_ERR_INVALID_ARG;
+    if (q == k || q == v || k == v) return ULYSSES_ERR_INVALID_ARG;
+    for (const void* a : ins)
+        if (!aligned16(a)) return ULYSSES_ERR_MISALIGNED;
+    for (const void* a : outs)
+        if (!aligned16(a)) return ULYSSES_ERR_MISALIGNED;
+    const int hq = shape.H * shape.d_h, hkv = shape_hkv(shape) * shape.d_h;
+    const int col0[4] = {0, hq, hq + hkv, hq + 2 * hkv};
+    void* out[3] = {q, k, v};
+    const int ld[3] = {hq, hkv, hkv};
+    return launch_proj_gemm(M, hq + 2 * hkv, hidden, x, w_qkv, 3, col0, out, ld, static_cast<cudaStream_t>(stream));
+}
+
+int ulysses_out_proj(ulysses_shape_t shape, int hidden, const void* o, const void* w_o, void* y, void* stream) {
+    int rc = validate_proj(shape, hidden);
+    if (rc != ULYSSES_OK) return rc;
+    const int M = shape.B * shape.L;
+    if (M == 0) return ULYSSES_OK;
+    if (!o || !w_o || !y) return ULYSSES_ERR_INVALID_ARG;
+    if (y == o || y == w_o) return ULYSSES_ERR_INVALID_ARG;
+    if (!aligned16(o) || !aligned16(w_o) || !aligned16(y)) return ULYSSES_ERR_MISALIGNED;
+    const int col0[2] = {0, hidden};
+    void* out[1] = {y};
+    const int ld[1] = {hidden};
+    return launch_proj_gemm(M, hidden, shape.H * shape.d_h, o, w_o, 1, col0, out, ld, static_cast<cudaStream_t>(stream));
 }
 
 int ulysses_attn_fwd(ulysses_shape_t shape, const ulysses_mask_t* mask, float softmax_scale, int io_layout,

@@ -16,7 +16,7 @@ namespace ulysses {
 //   bits 31..24 kernel id, 23..16 role, 15..0 wait site.
 // ---------------------------------------------------------------------------------------
 
-enum : uint32_t { KID_FWD = 1, KID_BWD = 2, KID_SELFTEST = 3 };
+enum : uint32_t { KID_FWD = 1, KID_BWD = 2, KID_SELFTEST = 3, KID_PROJ = 4 };
 enum : uint32_t { ROLE_LOAD = 1, ROLE_MMA = 2, ROLE_SOFTMAX = 3, ROLE_DQ = 4, ROLE_EPI = 5, ROLE_SELFTEST = 6 };
 
 // A wait gives up after this many nanoseconds of %globaltimer.
@@ -120,6 +120,14 @@ __device__ __forceinline__ void tma_load_5d(void* smem_dst, const CUtensorMap* m
         " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
         ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2),
           "r"(c3), "r"(c4), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
 }
 

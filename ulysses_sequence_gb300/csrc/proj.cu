@@ -1,0 +1,210 @@
+// The projections on either side of the Ulysses attention block (paper summary section 3.2
+// "Big-Picture Architecture" and section 3.4.1 "Before attention"; pinyu.ai page "One
+// attention block, end to end"): each rank projects its own token shard to Q, K, V before
+// the first all-to-all, and projects the returned O after the second. Every token row is
+// projected on its own, so on the token-sharded layout [P][B][Lp][features] both are one
+// matrix product over the rows, C[M][N] = A[M][K] B[N][K]^T (M = B L token rows, weights
+// in the y = x W^T convention):
+//   QKV projection:  A = X [M][hidden], B = W_qkv [(H + 2 Hkv) d][hidden]; the epilogue
+//                    writes columns [0, H d) to Q, [H d, (H + Hkv) d) to K and the rest
+//                    to V, each row-major, i.e. directly in the token-sharded layout the
+//                    attention kernels read (no relayout pass);
+//   out projection:  A = O [M][H d], B = W_o [hidden][H d], C = Y [M][hidden].
+//
+// One CTA computes a 128 x 256 tile of C on the 5th-generation tensor cores: warp 0 loads
+// A and B K-slices of 64 through a 4-stage TMA ring, warp 1 issues M128 N256 K16 MMAs
+// into a TMEM accumulator (256 columns), warps 2-5 convert the accumulator to bf16 and
+// store it. Tiles are rasterized in groups of 8 row tiles, so the CTAs resident at one
+// time share their A and B slices in L2.
+#include "common.cuh"
+#include "ulysses_internal.h"
+
+namespace ulysses {
+
+struct GemmCfg {
+    static constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, GROUP_M = 8;
+    static constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
+    static constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t OFF_BAR = STAGES * STAGE_BYTES;
+    static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
+    static constexpr uint32_t TMEM_COLS = 256;
+    static constexpr int kThreads = 192;
+};
+
+struct GemmParams {
+    int M, N, K;
+    int n_out;          // column ranges of C written to separate outputs (1 or 3)
+    int col0[4];        // range i is columns [col0[i], col0[i + 1])
+    void* out[3];       // bf16, row-major
+    int ld[3];          // row pitch of each output in elements
+    uint32_t* err;
+};
+
+__global__ void __launch_bounds__(GemmCfg::kThreads, 1)
+proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, const GemmParams p) {
+    using C = GemmCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* full = bars;                  // [STAGES]
+    uint64_t* empty = bars + C::STAGES;     // [STAGES]
+    uint64_t* acc_full = bars + 2 * C::STAGES;
+    uint64_t* drain = acc_full + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const int warp = static_cast<int>(warp_id());
+    const int lane = static_cast<int>(lane_id());
+    // grouped raster: GROUP_M row tiles vary fastest, then column tiles, then groups
+    const int tiles_m = (p.M + C::BM - 1) / C::BM, tiles_n = (p.N + C::BN - 1) / C::BN;
+    const int t = blockIdx.x;
+    const int per_group = C::GROUP_M * tiles_n;
+    const int group = t / per_group;
+    const int gm = min(C::GROUP_M, tiles_m - group * C::GROUP_M);  // row tiles in this group
+    const int in_group = t - group * per_group;
+    const int m0 = (group * C::GROUP_M + in_group % gm) * C::BM;
+    const int n0 = (in_group / gm) * C::BN;
+    const int n_k = (p.K + C::BK - 1) / C::BK;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::STAGES; ++i) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Abort ab{abort_flag, p.err, KID_PROJ};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_a);
+            tma_prefetch_desc(&tm_b);
+            int issued = 0;
+            bool ok = true;
+            for (int ks = 0; ks < n_k; ++ks) {
+                const int s = ks % C::STAGES;
+                if (ks >= C::STAGES && !(ok = mbar_wait(empty + s, ((ks / C::STAGES) - 1) & 1, ab, ROLE_LOAD, 1)))
+                    break;
+                uint8_t* st = smem + s * C::STAGE_BYTES;
+                mbar_arrive_expect_tx(full + s, C::STAGE_BYTES);
+                tma_load_2d(st, &tm_a, full + s, ks * C::BK, m0);
+                tma_load_2d(st + C::A_BYTES, &tm_b, full + s, ks * C::BK, n0);
+                ++issued;
+            }
+            if (!ok) {
+                for (int s = 0; s < C::STAGES; ++s) {
+                    const int cnt = issued > s ? (issued - 1 - s) / C::STAGES + 1 : 0;
+                    if (cnt > 0) mbar_drain(full + s, (cnt - 1) & 1);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(C::BM, C::BN, 0, 0);
+            const uint32_t base = smem_u32(smem);
+            bool ok = true;
+            for (int ks = 0; ks < n_k; ++ks) {
+                const int s = ks % C::STAGES;
+                if (!(ok = mbar_wait(full + s, (ks / C::STAGES) & 1, ab, ROLE_MMA, 1))) break;
+                tc_fence_after();
+                const uint64_t da = sdesc_sw128(base + s * C::STAGE_BYTES, 16, 1024);
+                const uint64_t db = sdesc_sw128(base + s * C::STAGE_BYTES + C::A_BYTES, 16, 1024);
+#pragma unroll
+                for (int k = 0; k < C::BK / 16; ++k)
+                    umma_ss(tmem, sdesc_add(da, k * 32), sdesc_add(db, k * 32), idesc, (ks > 0 || k > 0) ? 1u : 0u);
+                umma_commit(empty + s);
+            }
+            if (ok) umma_commit(acc_full);
+            else {
+                umma_commit(drain);
+                mbar_drain(drain, 0);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        // thread = one row of the tile (TMEM lane); 32-column chunks go to the output that
+        // holds them (the column ranges are multiples of 32 wide)
+        const int wq = warp & 3;
+        const int row = m0 + wq * 32 + lane;
+        const uint32_t lane_off = uint32_t(wq * 32) << 16;
+        const bool ok = n_k > 0 && __all_sync(0xffffffffu, mbar_wait(acc_full, 0, ab, ROLE_EPI, 1));
+        if (ok) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < C::BN; c += 32) {
+                const int col = n0 + c;
+                if (col >= p.N) break;  // warp-uniform
+                float v[32];
+                tmem_ld32(tmem + lane_off + c, v);
+                tmem_wait_ld();
+                int o = 0;
+                while (o + 1 < p.n_out && col >= p.col0[o + 1]) ++o;
+                if (row < p.M) {
+                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out[o]) + size_t(row) * p.ld[o] + (col - p.col0[o]);
+                    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+                        d4[x] = make_uint4(pack_bf16(v[8 * x], v[8 * x + 1]), pack_bf16(v[8 * x + 2], v[8 * x + 3]),
+                                           pack_bf16(v[8 * x + 4], v[8 * x + 5]), pack_bf16(v[8 * x + 6], v[8 * x + 7]));
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncwarp();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// 2-D bf16 tensor map over a row-major [rows][cols] matrix with a (64, box_rows) box and the
+// 128-byte swizzle, zero fill out of bounds.
+static bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return encode_tensor_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr);
+}
+
+int launch_proj_gemm(int M, int N, int K, const void* a, const void* b, int n_out, const int* col0, void* const* out,
+                     const int* ld, cudaStream_t stream) {
+    using C = GemmCfg;
+    GemmParams p{};
+    p.M = M; p.N = N; p.K = K; p.n_out = n_out;
+    for (int i = 0; i <= n_out; ++i) p.col0[i] = col0[i];
+    for (int i = 0; i < n_out; ++i) { p.out[i] = out[i]; p.ld[i] = ld[i]; }
+    p.err = device_error_word();
+    if (!p.err) return ULYSSES_ERR_CUDA;
+    CUtensorMap ma, mb;
+    if (!encode_2d(&ma, a, uint64_t(M), uint64_t(K), C::BM) || !encode_2d(&mb, b, uint64_t(N), uint64_t(K), C::BN))
+        return ULYSSES_ERR_CUDA;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_set[dev & 63]) {
+        if (cudaFuncSetAttribute(proj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+            cudaSuccess)
+            return ULYSSES_ERR_CUDA;
+        attr_set[dev & 63] = true;
+    }
+    const int tiles = ((M + C::BM - 1) / C::BM) * ((N + C::BN - 1) / C::BN);
+    proj_gemm_kernel<<<tiles, C::kThreads, C::SMEM_BYTES, stream>>>(ma, mb, p);
+    return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
+}
+
+}  // namespace ulysses

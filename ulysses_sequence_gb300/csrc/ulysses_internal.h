@@ -32,6 +32,12 @@ inline KvInfo kv_info(const ulysses_shape_t& s) {
     return k;
 }
 
+// cuTensorMapEncodeTiled (looked up at run time) with the 128-byte swizzle, 256-byte L2
+// promotion and zero fill out of bounds.
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
+                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                       const cuuint32_t* elem_strides);
+
 // Encodes a 5-D bf16 tensor map over (d, head, row, batch, unit) with a box of
 // (64, 1, box_rows, 1, 1), 128-byte swizzle and zero fill out of bounds, for a tensor with
 // `heads` heads in the token layout and `group_heads` per head group in the head layout:
@@ -59,6 +65,11 @@ int launch_attn_bwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, in
                     void* dk, void* dv, void* workspace, cudaStream_t stream);
 
 size_t bwd_workspace_bytes(const ulysses_shape_t& s);
+
+// C[M][N] = A[M][K] B[N][K]^T in bf16 (fp32 accumulation); column range [col0[i], col0[i+1])
+// of C is written row-major to out[i] with row pitch ld[i].
+int launch_proj_gemm(int M, int N, int K, const void* a, const void* b, int n_out, const int* col0, void* const* out,
+                     const int* ld, cudaStream_t stream);
 
 inline int gcd_int(int a, int b) {
     while (b) { int t = a % b; a = b; b = t; }

@@ -119,6 +119,21 @@ def draw(B: int, L: int, H: int, d: int, P: int, seed: int, names: Iterable[str]
     return out
 
 
+def draw_weight(n_out: int, n_in: int, seed: int) -> torch.Tensor:
+    """A bf16 projection weight [n_out][n_in] (the y = x W^T convention): fp32 N(0, 1) / sqrt(n_in)
+    from its own CPU generator, rounded to nearest-even. The scale keeps projected values near
+    unit size, as a trained layer's initialisation would."""
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn((n_out, n_in), generator=g, dtype=torch.float32) / math.sqrt(n_in)).to(torch.bfloat16)
+
+
+def draw_hidden(B: int, L: int, hidden: int, P: int, seed: int) -> torch.Tensor:
+    """Token-sharded bf16 hidden states [P][B][L/P][hidden], fp32 N(0, 1) rounded to nearest-even."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((B, L, hidden), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return x.reshape(B, P, L // P, hidden).permute(1, 0, 2, 3).contiguous()
+
+
 def draw_workload(w: Workload, names: Iterable[str] = ("q", "k", "v", "do")) -> Dict[str, torch.Tensor]:
     return draw(w.B, w.L, w.H, w.d, w.P, w.seed, names, q_scale=w.q_scale, H_kv=w.H_kv)
 
