@@ -11,11 +11,12 @@
 //                    attention kernels read (no relayout pass);
 //   out projection:  A = O [M][H d], B = W_o [hidden][H d], C = Y [M][hidden].
 //
-// One CTA computes a 128 x 256 tile of C on the 5th-generation tensor cores: warp 0 loads
-// A and B K-slices of 64 through a 4-stage TMA ring, warp 1 issues M128 N256 K16 MMAs
-// into a TMEM accumulator (256 columns), warps 2-5 convert the accumulator to bf16 and
-// store it. Tiles are rasterized in groups of 8 row tiles, so the CTAs resident at one
-// time share their A and B slices in L2.
+// A persistent CTA per SM walks 128 x 256 tiles of C on the 5th-generation tensor cores:
+// warp 0 loads A and B K-slices of 64 through a 4-stage TMA ring that runs on across tiles,
+// warp 1 issues M128 N256 K16 MMAs into one of two TMEM accumulators (256 columns each),
+// warps 2-5 convert the other accumulator to bf16 and store it, so a tile's epilogue
+// overlaps the next tile's MMAs. Tiles are rasterized in groups of 8 row tiles, so the
+// tiles in flight at one time share their A and B slices in L2.
 #include "common.cuh"
 #include "ulysses_internal.h"
 
@@ -28,7 +29,7 @@ struct GemmCfg {
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t OFF_BAR = STAGES * STAGE_BYTES;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
-    static constexpr uint32_t TMEM_COLS = 256;
+    static constexpr uint32_t TMEM_COLS = 512;  // two accumulators
     static constexpr int kThreads = 192;
 };
 
@@ -49,30 +50,36 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* full = bars;                  // [STAGES]
     uint64_t* empty = bars + C::STAGES;     // [STAGES]
-    uint64_t* acc_full = bars + 2 * C::STAGES;
-    uint64_t* drain = acc_full + 1;
+    uint64_t* acc_full = bars + 2 * C::STAGES;   // [2]
+    uint64_t* acc_empty = acc_full + 2;          // [2], 4 epilogue warps
+    uint64_t* drain = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = static_cast<int>(warp_id());
     const int lane = static_cast<int>(lane_id());
-    // grouped raster: GROUP_M row tiles vary fastest, then column tiles, then groups
     const int tiles_m = (p.M + C::BM - 1) / C::BM, tiles_n = (p.N + C::BN - 1) / C::BN;
-    const int t = blockIdx.x;
-    const int per_group = C::GROUP_M * tiles_n;
-    const int group = t / per_group;
-    const int gm = min(C::GROUP_M, tiles_m - group * C::GROUP_M);  // row tiles in this group
-    const int in_group = t - group * per_group;
-    const int m0 = (group * C::GROUP_M + in_group % gm) * C::BM;
-    const int n0 = (in_group / gm) * C::BN;
+    const int n_tiles = tiles_m * tiles_n;
     const int n_k = (p.K + C::BK - 1) / C::BK;
+    // grouped raster: GROUP_M row tiles vary fastest, then column tiles, then groups
+    auto tile_origin = [&](int t, int& m0, int& n0) {
+        const int per_group = C::GROUP_M * tiles_n;
+        const int group = t / per_group;
+        const int gm = min(C::GROUP_M, tiles_m - group * C::GROUP_M);  // row tiles in this group
+        const int in_group = t - group * per_group;
+        m0 = (group * C::GROUP_M + in_group % gm) * C::BM;
+        n0 = (in_group / gm) * C::BN;
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::STAGES; ++i) {
             mbar_init(full + i, 1);
             mbar_init(empty + i, 1);
         }
-        mbar_init(acc_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(acc_full + i, 1);
+            mbar_init(acc_empty + i, 4);
+        }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -89,17 +96,21 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         if (lane == 0) {
             tma_prefetch_desc(&tm_a);
             tma_prefetch_desc(&tm_b);
-            int issued = 0;
+            int issued = 0;  // K-slices loaded so far, over all of this CTA's tiles
             bool ok = true;
-            for (int ks = 0; ks < n_k; ++ks) {
-                const int s = ks % C::STAGES;
-                if (ks >= C::STAGES && !(ok = mbar_wait(empty + s, ((ks / C::STAGES) - 1) & 1, ab, ROLE_LOAD, 1)))
-                    break;
-                uint8_t* st = smem + s * C::STAGE_BYTES;
-                mbar_arrive_expect_tx(full + s, C::STAGE_BYTES);
-                tma_load_2d(st, &tm_a, full + s, ks * C::BK, m0);
-                tma_load_2d(st + C::A_BYTES, &tm_b, full + s, ks * C::BK, n0);
-                ++issued;
+            for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+                int m0, n0;
+                tile_origin(t, m0, n0);
+                for (int ks = 0; ks < n_k; ++ks, ++issued) {
+                    const int s = issued % C::STAGES;
+                    if (issued >= C::STAGES &&
+                        !(ok = mbar_wait(empty + s, ((issued / C::STAGES) - 1) & 1, ab, ROLE_LOAD, 1)))
+                        break;
+                    uint8_t* st = smem + s * C::STAGE_BYTES;
+                    mbar_arrive_expect_tx(full + s, C::STAGE_BYTES);
+                    tma_load_2d(st, &tm_a, full + s, ks * C::BK, m0);
+                    tma_load_2d(st + C::A_BYTES, &tm_b, full + s, ks * C::BK, n0);
+                }
             }
             if (!ok) {
                 for (int s = 0; s < C::STAGES; ++s) {
@@ -114,19 +125,27 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             constexpr uint32_t idesc = idesc_bf16(C::BM, C::BN, 0, 0);
             const uint32_t base = smem_u32(smem);
             bool ok = true;
-            for (int ks = 0; ks < n_k; ++ks) {
-                const int s = ks % C::STAGES;
-                if (!(ok = mbar_wait(full + s, (ks / C::STAGES) & 1, ab, ROLE_MMA, 1))) break;
+            int used = 0;  // K-slices consumed so far
+            for (int t = blockIdx.x, i = 0; ok && t < n_tiles; t += gridDim.x, ++i) {
+                const int a = i & 1;
+                // the epilogue must have read this accumulator's previous tile
+                if (i >= 2 && !(ok = mbar_wait(acc_empty + a, ((i >> 1) - 1) & 1, ab, ROLE_MMA, 2))) break;
                 tc_fence_after();
-                const uint64_t da = sdesc_sw128(base + s * C::STAGE_BYTES, 16, 1024);
-                const uint64_t db = sdesc_sw128(base + s * C::STAGE_BYTES + C::A_BYTES, 16, 1024);
+                const uint32_t acc = tmem + a * C::BN;
+                for (int ks = 0; ks < n_k; ++ks, ++used) {
+                    const int s = used % C::STAGES;
+                    if (!(ok = mbar_wait(full + s, (used / C::STAGES) & 1, ab, ROLE_MMA, 1))) break;
+                    tc_fence_after();
+                    const uint64_t da = sdesc_sw128(base + s * C::STAGE_BYTES, 16, 1024);
+                    const uint64_t db = sdesc_sw128(base + s * C::STAGE_BYTES + C::A_BYTES, 16, 1024);
 #pragma unroll
-                for (int k = 0; k < C::BK / 16; ++k)
-                    umma_ss(tmem, sdesc_add(da, k * 32), sdesc_add(db, k * 32), idesc, (ks > 0 || k > 0) ? 1u : 0u);
-                umma_commit(empty + s);
+                    for (int k = 0; k < C::BK / 16; ++k)
+                        umma_ss(acc, sdesc_add(da, k * 32), sdesc_add(db, k * 32), idesc, (ks > 0 || k > 0) ? 1u : 0u);
+                    umma_commit(empty + s);
+                }
+                if (ok) umma_commit(acc_full + a);
             }
-            if (ok) umma_commit(acc_full);
-            else {
+            if (!ok) {
                 umma_commit(drain);
                 mbar_drain(drain, 0);
             }
@@ -136,17 +155,21 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         // thread = one row of the tile (TMEM lane); 32-column chunks go to the output that
         // holds them (the column ranges are multiples of 32 wide)
         const int wq = warp & 3;
-        const int row = m0 + wq * 32 + lane;
         const uint32_t lane_off = uint32_t(wq * 32) << 16;
-        const bool ok = n_k > 0 && __all_sync(0xffffffffu, mbar_wait(acc_full, 0, ab, ROLE_EPI, 1));
-        if (ok) {
+        for (int t = blockIdx.x, i = 0; n_k > 0 && t < n_tiles; t += gridDim.x, ++i) {
+            const int a = i & 1;
+            int m0, n0;
+            tile_origin(t, m0, n0);
+            if (!__all_sync(0xffffffffu, mbar_wait(acc_full + a, (i >> 1) & 1, ab, ROLE_EPI, 1))) break;
             tc_fence_after();
+            const int row = m0 + wq * 32 + lane;
+            const uint32_t acc = tmem + lane_off + a * C::BN;
 #pragma unroll 1
             for (int c = 0; c < C::BN; c += 32) {
                 const int col = n0 + c;
                 if (col >= p.N) break;  // warp-uniform
                 float v[32];
-                tmem_ld32(tmem + lane_off + c, v);
+                tmem_ld32(acc + c, v);
                 tmem_wait_ld();
                 int o = 0;
                 while (o + 1 < p.n_out && col >= p.col0[o + 1]) ++o;
@@ -159,6 +182,10 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                                            pack_bf16(v[8 * x + 4], v[8 * x + 5]), pack_bf16(v[8 * x + 6], v[8 * x + 7]));
                 }
             }
+            // this accumulator may take the next tile but one
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty + a);
         }
     }
 
@@ -203,7 +230,8 @@ int launch_proj_gemm(int M, int N, int K, const void* a, const void* b, int n_ou
         attr_set[dev & 63] = true;
     }
     const int tiles = ((M + C::BM - 1) / C::BM) * ((N + C::BN - 1) / C::BN);
-    proj_gemm_kernel<<<tiles, C::kThreads, C::SMEM_BYTES, stream>>>(ma, mb, p);
+    const int grid = tiles < device_sm_count() ? tiles : device_sm_count();  // persistent: one CTA per SM
+    proj_gemm_kernel<<<grid, C::kThreads, C::SMEM_BYTES, stream>>>(ma, mb, p);
     return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }
 
