@@ -145,3 +145,20 @@ def test_grouped_kv_head_counts_are_validated(lib):
     for hkv in (8, 4, 2, 1):
         assert U.ulysses_attn_bwd_workspace_size(U.Shape(1, 256, 8, 64, 4, hkv)) > 0
     assert U.ulysses_kv_seq_to_head(U.Shape(0, 256, 8, 64, 4, 2), 0, 0, 0) == U.OK   # empty batch
+
+
+def test_projection_argument_checks(lib):
+    """The projections validate sizes, pointers and alignment on the host, before any launch."""
+    s = U.Shape(1, 256, 8, 64, 4)
+    p = [256 * (i + 1) for i in range(5)]
+    assert U.ulysses_qkv_proj(s, 0, *p, 0) == U.ERR_INVALID_ARG                      # hidden 0
+    assert U.ulysses_qkv_proj(s, 48, *p, 0) == U.ERR_UNSUPPORTED                     # hidden % 32
+    assert U.ulysses_qkv_proj(U.Shape(1, 256, 6, 64, 4), 512, *p, 0) == U.ERR_INVALID_ARG  # H % P
+    assert U.ulysses_qkv_proj(s, 512, 0, *p[1:], 0) == U.ERR_INVALID_ARG             # null x
+    assert U.ulysses_qkv_proj(s, 512, p[0], p[1], p[0], p[3], p[4], 0) == U.ERR_INVALID_ARG  # q aliases x
+    assert U.ulysses_qkv_proj(s, 512, p[0], p[1], p[2], p[2], p[4], 0) == U.ERR_INVALID_ARG  # q == k
+    assert U.ulysses_qkv_proj(s, 512, p[0] + 8, *p[1:], 0) == U.ERR_MISALIGNED       # x not 16-aligned
+    assert U.ulysses_qkv_proj(U.Shape(0, 256, 8, 64, 4), 512, 0, 0, 0, 0, 0, 0) == U.OK  # empty batch
+    assert U.ulysses_out_proj(s, 512, p[0], p[1], p[0], 0) == U.ERR_INVALID_ARG      # y aliases o
+    assert U.ulysses_out_proj(s, 512, p[0], p[1], p[2] + 2, 0) == U.ERR_MISALIGNED
+    assert U.ulysses_out_proj(s, 40, *p[:3], 0) == U.ERR_UNSUPPORTED
