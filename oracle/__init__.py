@@ -317,6 +317,26 @@ def attention_full(q_tok: np.ndarray, k_tok: np.ndarray, v_tok: np.ndarray, P: i
     return out
 
 
+# --------------------------------------------------------------------------- ring merge
+
+def merge_partials(o_parts, lse_parts):
+    """Combine attention results over disjoint key sets into the result over their union (the
+    online-softmax rule that ring attention streams K/V blocks with; pages' Ring Attention /
+    USP hybrid): with m = max_j lse_j, w_j = exp(lse_j - m),
+        lse = m + ln sum_j w_j,   O = sum_j w_j O_j / sum_j w_j.
+    o_parts: list of [..., n, d] arrays, lse_parts: list of matching [..., n] arrays (same
+    leading shape). A row with lse = -inf in every part gets O = 0 and lse = -inf."""
+    lse = np.stack([np.asarray(x, dtype=np.float64) for x in lse_parts])      # [J, ..., n]
+    o = np.stack([np.asarray(x, dtype=np.float64) for x in o_parts])          # [J, ..., n, d]
+    m = lse.max(axis=0)
+    finite = np.isfinite(m)
+    w = np.where(finite, np.exp(lse - np.where(finite, m, 0.0)), 0.0)
+    tot = w.sum(axis=0)
+    out_lse = np.where(finite, m + np.log(np.where(finite, tot, 1.0)), -np.inf)
+    out_o = np.where(finite[..., None], (w[..., None] * o).sum(axis=0) / np.where(finite, tot, 1.0)[..., None], 0.0)
+    return out_o, out_lse
+
+
 # --------------------------------------------------------------------------- projections
 
 def _as_f64(x: np.ndarray) -> np.ndarray:

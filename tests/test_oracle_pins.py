@@ -446,3 +446,31 @@ def test_projection_of_shards_equals_projection_of_the_sequence():
         for n in ("q", "k", "v"):
             merged = out[n].transpose(1, 0, 2, 3, 4).reshape(B, L, H, d)
             np.testing.assert_allclose(merged, ref[n][0], rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- ring merge
+
+@pytest.mark.parametrize("n_parts", [1, 2, 3])
+def test_merge_of_key_subsets_equals_attention_over_their_union(n_parts):
+    """Attention over a key set, split into disjoint subsets, equals the merge of the
+    attention results over each subset (lse and O) -- the identity ring attention relies on."""
+    L, d = 24, 8
+    q, k, v = RNG.standard_normal((L, d)), RNG.standard_normal((L, d)), RNG.standard_normal((L, d))
+    rows = np.arange(L)
+    full_o, full_lse = oracle.head_forward(q, k, v, rows, Mask("none"), 1.0 / math.sqrt(d))
+    cuts = np.array_split(np.random.default_rng(n_parts).permutation(L), n_parts)
+    parts = []
+    for keys in cuts:
+        o_j, l_j = oracle.head_forward(q, k[keys], v[keys], rows, Mask("none"), 1.0 / math.sqrt(d))
+        parts.append((o_j, l_j))
+    o, lse = oracle.merge_partials([p[0] for p in parts], [p[1] for p in parts])
+    np.testing.assert_allclose(o, full_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, full_lse, rtol=0, atol=1e-12)
+
+
+def test_merge_with_an_empty_part_and_an_empty_row():
+    o1, l1 = np.ones((2, 3)), np.array([0.5, -np.inf])
+    o2, l2 = np.zeros((2, 3)), np.array([-np.inf, -np.inf])
+    o, lse = oracle.merge_partials([o1, o2], [l1, l2])
+    np.testing.assert_array_equal(o, [[1, 1, 1], [0, 0, 0]])
+    assert lse[0] == 0.5 and np.isneginf(lse[1])
