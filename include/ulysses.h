@@ -215,6 +215,30 @@ int ulysses_qkv_proj(ulysses_shape_t shape, int hidden, const void *x, const voi
  * w_o [hidden][H d_h]; writes y [P][B][Lp][hidden]. Same requirements. */
 int ulysses_out_proj(ulysses_shape_t shape, int hidden, const void *o, const void *w_o, void *y, void *stream);
 
+/* Ulysses-ring hybrid (the aifetchly page's step 5, "USP"; Ring Attention in the reading notes,
+ * section 5.2), which lifts the P <= H limit of the head cut: P = P_u * P_ring. The sequence is
+ * cut into P_ring ring blocks of L / P_ring tokens, i.e. P_u = P / P_ring consecutive token
+ * shards each. Inside a block the Ulysses relayout spreads the heads over P_u head groups (so
+ * P_u, not P, must divide H); across blocks each query block meets every key/value block, and
+ * the block results are merged with the online-softmax rule (m = max lse_j, lse = m +
+ * ln sum exp(lse_j - m), O = sum exp(lse_j - lse) O_j).
+ * q, k, v, o, dO, dq, dk, dv: TOKEN_SHARDED [P][B][Lp][H (or H_kv)][d_h] as for
+ * ulysses_attn_fwd with P shards. lse: fp32, per ring block the layout of that block's
+ * attention, [P_ring][P_u][B][H / P_u][L / P_ring]. Masks: causal (by global token position) or
+ * none; block-sparse gives ULYSSES_ERR_UNSUPPORTED. P_ring <= 64 and P % P_ring == 0; every
+ * ring block must be a valid ulysses_attn_fwd shape. workspace: at least
+ * ulysses_usp_workspace_size(shape, P_ring) bytes, 256-byte aligned (0 for invalid shapes). The
+ * backward sums partial gradients over block pairs in fp32, so all its outputs are deterministic
+ * up to the reduction order of each block pair's dQ. */
+size_t ulysses_usp_workspace_size(ulysses_shape_t shape, int P_ring);
+int ulysses_usp_attn_fwd(ulysses_shape_t shape, int P_ring, const ulysses_mask_t *mask, float softmax_scale,
+                         const void *q, const void *k, const void *v, void *o, float *lse, void *workspace,
+                         size_t workspace_bytes, void *stream);
+int ulysses_usp_attn_bwd(ulysses_shape_t shape, int P_ring, const ulysses_mask_t *mask, float softmax_scale,
+                         const void *q, const void *k, const void *v, const void *o, const float *lse,
+                         const void *dO, void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
 /* Host helper: the block-sparse pattern "sliding window plus strided global key tiles".
  * Query tile qt gets key tiles max(0, qt - window_before) .. min(n - 1, qt + window_after)
  * and every kt with kt % global_stride == 0 (global_stride <= 0: none), n = ceil(L/tile).

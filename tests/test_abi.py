@@ -162,3 +162,30 @@ def test_projection_argument_checks(lib):
     assert U.ulysses_out_proj(s, 512, p[0], p[1], p[0], 0) == U.ERR_INVALID_ARG      # y aliases o
     assert U.ulysses_out_proj(s, 512, p[0], p[1], p[2] + 2, 0) == U.ERR_MISALIGNED
     assert U.ulysses_out_proj(s, 40, *p[:3], 0) == U.ERR_UNSUPPORTED
+
+
+def test_usp_argument_checks(lib):
+    """The Ulysses-ring hybrid validates the split P = P_u * P_ring on the host: P_ring must
+    divide P, each ring block must be a valid token-sharded attention shape (P_u | H, Lp % 8),
+    block-sparse masks are not supported, the workspace is sized and 256-byte aligned."""
+    m = U.MaskStruct(U.MASK_CAUSAL, 128, None, None, None, None, 0)
+    s = U.Shape(1, 512, 4, 128, 8)                 # P = 8 > H = 4: only valid with P_ring >= 2
+    need = U.ulysses_usp_workspace_size(s, 2)
+    assert need > 0 and need % 256 == 0
+    assert U.ulysses_usp_workspace_size(s, 1) == 0                               # P_u = 8 does not divide H
+    assert U.ulysses_usp_workspace_size(s, 3) == 0                               # 3 does not divide 8
+    assert U.ulysses_usp_workspace_size(s, 0) == 0
+    assert U.ulysses_usp_workspace_size(U.Shape(1, 512, 4, 96, 8), 2) == 0       # d_h 96
+    p = [256 * (i + 1) for i in range(10)]
+    ws = 1 << 20
+    assert U.ulysses_usp_attn_fwd(s, 2, m, 0.0, *p[:5], ws, need - 256, 0) == U.ERR_INVALID_ARG
+    assert U.ulysses_usp_attn_fwd(s, 2, m, 0.0, *p[:5], ws + 64, need, 0) == U.ERR_MISALIGNED
+    assert U.ulysses_usp_attn_fwd(s, 2, m, 0.0, p[0], p[1], p[2], p[0], p[4], ws, need, 0) == U.ERR_INVALID_ARG
+    assert U.ulysses_usp_attn_fwd(s, 2, m, 0.0, p[0] + 8, *p[1:5], ws, need, 0) == U.ERR_MISALIGNED
+    assert U.ulysses_usp_attn_fwd(s, 1, m, 0.0, *p[:5], ws, need, 0) == U.ERR_INVALID_ARG
+    sparse = U.MaskStruct(U.MASK_BLOCK_SPARSE, 128, 16, 16, 16, 16, 1)
+    assert U.ulysses_usp_attn_fwd(s, 2, sparse, 0.0, *p[:5], ws, need, 0) == U.ERR_UNSUPPORTED
+    assert U.ulysses_usp_attn_fwd(U.Shape(0, 512, 4, 128, 8), 2, m, 0.0, 0, 0, 0, 0, 0, 0, 0, 0) == U.OK
+    assert U.ulysses_usp_attn_bwd(s, 2, m, 0.0, *p[:9], ws, need - 256, 0) == U.ERR_INVALID_ARG
+    assert U.ulysses_usp_attn_bwd(s, 2, m, 0.0, *p[:6], p[0], p[7], p[8], ws, need, 0) == U.ERR_INVALID_ARG  # dq aliases q
+    assert U.ulysses_usp_attn_bwd(s, 2, m, 0.0, *p[:8], p[7], ws, need, 0) == U.ERR_INVALID_ARG   # dk == dv

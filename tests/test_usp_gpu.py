@@ -1,0 +1,124 @@
+"""GPU parity of the Ulysses-ring hybrid (USP) through the C ABI against the fp64 oracle.
+
+P = P_u * P_ring token shards: ring blocks of L / P_ring tokens, each spread over P_u head
+groups by the Ulysses relayout, per-block-pair attention merged by the online-softmax rule.
+Whatever the split, the result is exact attention over the whole sequence, so the oracle is
+attention over all L tokens at once (one shard). Checked on every row: causal and dense masks,
+P > H (the case the hybrid exists for), pure ring (P_u = 1), grouped key/value heads, d_h 64,
+a ragged tail inside each ring block, and P_ring = 1 equal to the plain Ulysses calls.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ulysses_sequence_gb300 as U
+import workloads
+from gpu_util import ErrStats, LSE_MAX_ABS, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _one_shard(x: np.ndarray) -> np.ndarray:
+    """[P][B][Lp][H][d] -> [1][B][L][H][d]: the same tokens as a single shard."""
+    P, B, Lp, H, d = x.shape
+    return np.ascontiguousarray(x.transpose(1, 0, 2, 3, 4).reshape(1, B, P * Lp, H, d))
+
+
+def _usp_lse_logical(lse: np.ndarray) -> np.ndarray:
+    """[P_ring][P_u][B][H/P_u][L/P_ring] -> [B][H][L]."""
+    Pr, Pu, B, Hpu, Lb = lse.shape
+    return lse.transpose(2, 1, 3, 0, 4).reshape(B, Pu * Hpu, Pr * Lb)
+
+
+def _run(B, L, H, Hkv, d, P, P_ring, kind, seed):
+    t = workloads.draw(B, L, H, d, P, seed, H_kv=Hkv)
+    bits = {n: workloads.to_bf16_bits(x) for n, x in t.items()}
+    one = {n: _one_shard(x) for n, x in bits.items()}
+    ref = oracle.attention_full(one["q"], one["k"], one["v"], 1, oracle.Mask(kind), do_tok=one["do"])
+    dev = {n: x.cuda() for n, x in t.items()}
+    mask = U.Mask.causal() if kind == "causal" else U.Mask.none()
+    o, lse = U.usp_attn_fwd(dev["q"], dev["k"], dev["v"], P, P_ring, mask)
+    dq, dk, dv = U.usp_attn_bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], P, P_ring, mask)
+    torch.cuda.synchronize()
+    st, word = U.device_status()
+    assert st == U.OK, hex(word)
+    got = {n: _one_shard(oracle.bf16_to_f64(_bits(x))) for n, x in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv))}
+    got["lse"] = _usp_lse_logical(lse.cpu().double().numpy())
+    ref["lse"] = ref["lse"][0]
+    return got, ref
+
+
+def _check(got, ref):
+    s = ErrStats("o")
+    s.add(got["o"], ref["o"])
+    s.check()
+    # dQ sums P_ring bf16 partials (dK, dV up to P_ring partials, each itself a sum over the G
+    # query heads of a key/value head) in fp32 before the final rounding: the bound adds half a
+    # bf16 unit of each partial, at most 2^-8 of the result's magnitude for partials of one sign
+    for n in ("dq", "dk", "dv"):
+        s = ErrStats(n)
+        s.add(got[n], ref[n])
+        s.check(max_abs=None)
+        err = np.abs(got[n] - ref[n])
+        assert np.all(err <= 2e-2 + 2.0 ** -8 * np.abs(ref[n])), (n, float(err.max()))
+    fin = np.isfinite(ref["lse"])
+    assert np.array_equal(np.isneginf(got["lse"]), np.isneginf(ref["lse"]))
+    assert np.abs(got["lse"][fin] - ref["lse"][fin]).max() <= LSE_MAX_ABS
+
+
+CASES = [
+    # name, B, L, H, H_kv, d, P, P_ring, mask
+    ("causal_p4_ring2", 1, 512, 4, 4, 128, 4, 2, "causal"),
+    ("p_gt_h_p8_h4", 1, 512, 4, 4, 128, 8, 2, "causal"),
+    ("pure_ring_p4", 1, 1024, 2, 2, 128, 4, 4, "causal"),
+    ("dense_gqa_d64_b2", 2, 384, 8, 2, 64, 4, 4, "none"),
+    ("ragged_block_gqa", 1, 640, 8, 4, 128, 4, 2, "causal"),
+    ("dense_ring3", 1, 768, 4, 4, 128, 6, 3, "none"),
+]
+
+
+@pytest.mark.parametrize("name,B,L,H,Hkv,d,P,P_ring,kind", CASES, ids=[c[0] for c in CASES])
+def test_usp_every_row(name, B, L, H, Hkv, d, P, P_ring, kind):
+    got, ref = _run(B, L, H, Hkv, d, P, P_ring, kind, seed=sum(map(ord, name)))
+    _check(got, ref)
+
+
+def test_usp_ring1_is_plain_ulysses():
+    """With one ring block the merge has one part of weight 1 and the gradient sums have one
+    term: O, lse, dK and dV equal the plain Ulysses results bit for bit (dQ's fp32 reductions
+    run in no fixed order, so it matches within the usual bound)."""
+    B, L, H, d, P = 1, 512, 8, 128, 4
+    t = {n: x.cuda() for n, x in workloads.draw(B, L, H, d, P, 23).items()}
+    mask = U.Mask.causal()
+    o1, lse1 = U.usp_attn_fwd(t["q"], t["k"], t["v"], P, 1, mask)
+    dq1, dk1, dv1 = U.usp_attn_bwd(t["q"], t["k"], t["v"], o1, lse1, t["do"], P, 1, mask)
+    o2, lse2 = U.attn_fwd(t["q"], t["k"], t["v"], P, mask)
+    dq2, dk2, dv2 = U.attn_bwd(t["q"], t["k"], t["v"], o2, lse2, t["do"], P, mask)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(lse1.reshape(-1), lse2.reshape(-1))
+    assert torch.equal(dk1.view(torch.int16), dk2.view(torch.int16))
+    assert torch.equal(dv1.view(torch.int16), dv2.view(torch.int16))
+    assert (dq1.float() - dq2.float()).abs().max().item() <= 2e-2
+
+
+def test_usp_rejects_bad_splits():
+    q = torch.zeros((8, 1, 64, 4, 128), dtype=torch.bfloat16, device="cuda")
+    mask = U.Mask.causal()
+    with pytest.raises(U.UlyssesError):
+        U.usp_attn_fwd(q, q, q, 8, 1, mask)   # P_u = 8 does not divide H = 4
+    with pytest.raises(U.UlyssesError):
+        U.usp_attn_fwd(q, q, q, 8, 3, mask)   # P_ring does not divide P
+    assert U.ulysses_usp_workspace_size(U.Shape(1, 512, 4, 128, 8, 0), 3) == 0
+    assert U.ulysses_usp_workspace_size(U.Shape(1, 512, 4, 128, 8, 0), 2) > 0

@@ -37,7 +37,8 @@ class MaskStruct(ctypes.Structure):
 
 
 EXPORTS = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_kv_seq_to_head", "ulysses_kv_head_to_seq_sum",
-           "ulysses_qkv_proj", "ulysses_out_proj", "ulysses_attn_fwd", "ulysses_attn_bwd_workspace_size",
+           "ulysses_qkv_proj", "ulysses_out_proj", "ulysses_usp_workspace_size", "ulysses_usp_attn_fwd",
+           "ulysses_usp_attn_bwd", "ulysses_attn_fwd", "ulysses_attn_bwd_workspace_size",
            "ulysses_attn_bwd", "ulysses_attn_bwd_noalloc", "ulysses_bsmask_build_window_global",
            "ulysses_get_device_status", "ulysses_selftest_timeout", "ulysses_status_string")
 BWD_NOALLOC_SCRATCH_BYTES = 96 * 1024 * 1024  # ULYSSES_BWD_NOALLOC_SCRATCH_BYTES
@@ -58,6 +59,11 @@ def load() -> ctypes.CDLL:
     lib.ulysses_head_to_seq.argtypes = [Shape, vp, vp, vp]
     lib.ulysses_kv_seq_to_head.argtypes = [Shape, vp, vp, vp]
     lib.ulysses_qkv_proj.argtypes = [Shape, i, vp, vp, vp, vp, vp, vp]
+    lib.ulysses_usp_workspace_size.argtypes = [Shape, i]
+    lib.ulysses_usp_workspace_size.restype = sz
+    lib.ulysses_usp_attn_fwd.argtypes = [Shape, i, ctypes.POINTER(MaskStruct), f, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ulysses_usp_attn_bwd.argtypes = [Shape, i, ctypes.POINTER(MaskStruct), f, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                         vp, sz, vp]
     lib.ulysses_out_proj.argtypes = [Shape, i, vp, vp, vp, vp]
     lib.ulysses_kv_head_to_seq_sum.argtypes = [Shape, vp, vp, vp]
     lib.ulysses_attn_fwd.argtypes = [Shape, ctypes.POINTER(MaskStruct), f, i, vp, vp, vp, vp, vp, vp]
@@ -74,7 +80,7 @@ def load() -> ctypes.CDLL:
     lib.ulysses_status_string.argtypes = [i]
     lib.ulysses_status_string.restype = ctypes.c_char_p
     for name in EXPORTS:
-        if name != "ulysses_attn_bwd_workspace_size" and name != "ulysses_status_string":
+        if name not in ("ulysses_attn_bwd_workspace_size", "ulysses_usp_workspace_size", "ulysses_status_string"):
             getattr(lib, name).restype = i
     _lib = lib
     return lib
@@ -108,6 +114,23 @@ def ulysses_qkv_proj(shape: Shape, hidden: int, x: int, w_qkv: int, q: int, k: i
 
 def ulysses_out_proj(shape: Shape, hidden: int, o: int, w_o: int, y: int, stream: int) -> int:
     return load().ulysses_out_proj(shape, hidden, o, w_o, y, stream)
+
+
+def ulysses_usp_workspace_size(shape: Shape, P_ring: int) -> int:
+    return load().ulysses_usp_workspace_size(shape, P_ring)
+
+
+def ulysses_usp_attn_fwd(shape: Shape, P_ring: int, mask: MaskStruct, softmax_scale: float, q: int, k: int, v: int,
+                         o: int, lse: int, workspace: int, workspace_bytes: int, stream: int) -> int:
+    return load().ulysses_usp_attn_fwd(shape, P_ring, _mref(mask), softmax_scale, q, k, v, o, lse, workspace,
+                                       workspace_bytes, stream)
+
+
+def ulysses_usp_attn_bwd(shape: Shape, P_ring: int, mask: MaskStruct, softmax_scale: float, q: int, k: int, v: int,
+                         o: int, lse: int, dO: int, dq: int, dk: int, dv: int, workspace: int, workspace_bytes: int,
+                         stream: int) -> int:
+    return load().ulysses_usp_attn_bwd(shape, P_ring, _mref(mask), softmax_scale, q, k, v, o, lse, dO, dq, dk, dv,
+                                       workspace, workspace_bytes, stream)
 
 
 def ulysses_attn_fwd(shape: Shape, mask: MaskStruct, softmax_scale: float, io_layout: int, q: int, k: int, v: int,
@@ -317,6 +340,44 @@ def out_proj(o, w_o, P: int, y=None, stream=None):
     check(ulysses_out_proj(Shape(B, Lp * P, H, d, P), hidden, o.data_ptr(), w_o.data_ptr(), y.data_ptr(),
                            _stream(stream)), "out_proj")
     return y
+
+
+def usp_workspace(q, P: int, P_ring: int, kv_heads: int = 0):
+    import torch
+    n = ulysses_usp_workspace_size(_shape_of(q, P, LAYOUT_TOKEN_SHARDED, kv_heads=kv_heads), P_ring)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+
+
+def usp_attn_fwd(q, k, v, P: int, P_ring: int, mask: Mask, scale: float = 0.0, o=None, lse=None, workspace=None,
+                 stream=None):
+    """Ulysses-ring hybrid forward on token-sharded q [P][B][Lp][H][d] (k, v with H_kv heads).
+    Returns (o, lse[P_ring][P/P_ring][B][H/(P/P_ring)][L/P_ring] fp32)."""
+    import torch
+    shape = _shape_of(q, P, LAYOUT_TOKEN_SHARDED, k)
+    Pu = P // P_ring
+    o = torch.empty_like(q) if o is None else o
+    if lse is None:
+        lse = torch.empty((P_ring, Pu, shape.B, shape.H // Pu, shape.L // P_ring), dtype=torch.float32,
+                          device=q.device)
+    ws = usp_workspace(q, P, P_ring, shape.H_kv) if workspace is None else workspace
+    check(ulysses_usp_attn_fwd(shape, P_ring, mask.struct, scale, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                               o.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)), "usp_attn_fwd")
+    return o, lse
+
+
+def usp_attn_bwd(q, k, v, o, lse, do, P: int, P_ring: int, mask: Mask, scale: float = 0.0, dq=None, dk=None, dv=None,
+                 workspace=None, stream=None):
+    """Ulysses-ring hybrid backward. Returns (dq, dk, dv)."""
+    import torch
+    shape = _shape_of(q, P, LAYOUT_TOKEN_SHARDED, k)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = usp_workspace(q, P, P_ring, shape.H_kv) if workspace is None else workspace
+    check(ulysses_usp_attn_bwd(shape, P_ring, mask.struct, scale, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                               o.data_ptr(), lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                               ws.data_ptr(), ws.numel(), _stream(stream)), "usp_attn_bwd")
+    return dq, dk, dv
 
 
 def attn_fwd(q, k, v, P: int, mask: Mask, layout: int = LAYOUT_TOKEN_SHARDED, scale: float = 0.0, o=None,

@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libulysses.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-I" + os.path.join(ROOT, "include")] + ARCH
-SOURCES = ["api.cu", "relayout.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_noalloc.cu", "proj.cu"]
+SOURCES = ["api.cu", "relayout.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_noalloc.cu", "proj.cu", "usp.cu"]
 
 
 def nvcc() -> str:

@@ -278,6 +278,66 @@ int ulysses_out_proj(ulysses_shape_t shape, int hidden, const void* o, const voi
     return launch_proj_gemm(M, hidden, shape.H * shape.d_h, o, w_o, 1, col0, out, ld, static_cast<cudaStream_t>(stream));
 }
 
+// Ulysses-ring hybrid: the full shape only needs L % P == 0 and P % P_ring == 0; each ring block
+// (L / P_ring tokens, P / P_ring shards) must be a valid token-sharded attention shape.
+static int validate_usp(const ulysses_shape_t& s, int P_ring, const ulysses_mask_t* mask) {
+    if (s.B < 0 || s.L < 0 || s.H <= 0 || s.d_h <= 0 || s.P <= 0 || s.H_kv < 0) return ULYSSES_ERR_INVALID_ARG;
+    if (P_ring <= 0 || P_ring > kMaxRing || s.P % P_ring != 0 || s.L % s.P != 0) return ULYSSES_ERR_INVALID_ARG;
+    if (!mask) return ULYSSES_ERR_INVALID_ARG;
+    if (mask->kind == ULYSSES_MASK_BLOCK_SPARSE) return ULYSSES_ERR_UNSUPPORTED;
+    ulysses_shape_t sub = s;
+    sub.L = s.L / P_ring;
+    sub.P = s.P / P_ring;
+    return validate_attn(sub, mask, ULYSSES_LAYOUT_TOKEN_SHARDED);
+}
+
+size_t ulysses_usp_workspace_size(ulysses_shape_t shape, int P_ring) {
+    ulysses_mask_t causal{ULYSSES_MASK_CAUSAL, kTile, nullptr, nullptr, nullptr, nullptr, 0};
+    if (validate_usp(shape, P_ring, &causal) != ULYSSES_OK) return 0;
+    return usp_workspace_bytes(shape, P_ring);
+}
+
+int ulysses_usp_attn_fwd(ulysses_shape_t shape, int P_ring, const ulysses_mask_t* mask, float softmax_scale,
+                         const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    int rc = validate_usp(shape, P_ring, mask);
+    if (rc != ULYSSES_OK) return rc;
+    if (shape.B == 0 || shape.L == 0) return ULYSSES_OK;
+    if (!q || !k || !v || !o || !lse || !workspace) return ULYSSES_ERR_INVALID_ARG;
+    if (o == q || o == k || o == v) return ULYSSES_ERR_INVALID_ARG;
+    if (workspace_bytes < usp_workspace_bytes(shape, P_ring)) return ULYSSES_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ULYSSES_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ULYSSES_ERR_MISALIGNED;
+    MaskArgs m{mask->kind, nullptr, nullptr, nullptr, nullptr};
+    return launch_usp_fwd(shape, P_ring, m, resolve_scale(softmax_scale, shape.d_h), q, k, v, o, lse, workspace,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int ulysses_usp_attn_bwd(ulysses_shape_t shape, int P_ring, const ulysses_mask_t* mask, float softmax_scale,
+                         const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                         void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = validate_usp(shape, P_ring, mask);
+    if (rc != ULYSSES_OK) return rc;
+    if (shape.B == 0 || shape.L == 0) return ULYSSES_OK;
+    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace) return ULYSSES_ERR_INVALID_ARG;
+    if (workspace_bytes < usp_workspace_bytes(shape, P_ring)) return ULYSSES_ERR_INVALID_ARG;
+    const void* ins[] = {q, k, v, o, lse, dO};
+    const void* outs[] = {dq, dk, dv, workspace};
+    for (const void* a : outs)
+        for (const void* b : ins)
+            if (a == b) return ULYSSES_ERR_INVALID_ARG;
+    if (dq == dk || dq == dv || dk == dv) return ULYSSES_ERR_INVALID_ARG;
+    for (const void* a : ins)
+        if (!aligned16(a)) return ULYSSES_ERR_MISALIGNED;
+    for (const void* a : outs)
+        if (!aligned16(a)) return ULYSSES_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ULYSSES_ERR_MISALIGNED;
+    MaskArgs m{mask->kind, nullptr, nullptr, nullptr, nullptr};
+    return launch_usp_bwd(shape, P_ring, m, resolve_scale(softmax_scale, shape.d_h), q, k, v, o, lse, dO, dq, dk, dv,
+                          workspace, static_cast<cudaStream_t>(stream));
+}
+
 int ulysses_attn_fwd(ulysses_shape_t shape, const ulysses_mask_t* mask, float softmax_scale, int io_layout,
                      const void* q, const void* k, const void* v, void* o, float* lse, void* stream) {
     int rc = validate_attn(shape, mask, io_layout);

@@ -66,6 +66,15 @@ int launch_attn_bwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, in
 
 size_t bwd_workspace_bytes(const ulysses_shape_t& s);
 
+// Ulysses-ring hybrid over P_ring ring blocks (P_ring <= kMaxRing)
+constexpr int kMaxRing = 64;
+size_t usp_workspace_bytes(const ulysses_shape_t& s, int P_ring);
+int launch_usp_fwd(const ulysses_shape_t& s, int P_ring, const MaskArgs& m, float scale, const void* q, const void* k,
+                   const void* v, void* o, float* lse, void* ws, cudaStream_t stream);
+int launch_usp_bwd(const ulysses_shape_t& s, int P_ring, const MaskArgs& m, float scale, const void* q, const void* k,
+                   const void* v, const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                   void* ws, cudaStream_t stream);
+
 // C[M][N] = A[M][K] B[N][K]^T in bf16 (fp32 accumulation); column range [col0[i], col0[i+1])
 // of C is written row-major to out[i] with row pitch ld[i].
 int launch_proj_gemm(int M, int N, int K, const void* a, const void* b, int n_out, const int* col0, void* const* out,
