@@ -44,9 +44,9 @@ METRIC = "Ulysses attn fwd+bwd TFLOP/s & % BF16 peak; relayout HBM GB/s"
 # profiles/attn_kernels_gpt7b.md. A figure is reported only while the kernel sources still
 # hash to the value recorded with it; after any change it reads as null until re-captured.
 NCU_TRAFFIC = {
-    "attn_bwd_kernel": {"bytes": 2648071424, "workload": "gpt7b", "sha": "e44e357b0f731c1e",
+    "attn_bwd_kernel": {"bytes": 2645222912, "workload": "gpt7b", "sha": "bd7b9efb74ce932f",
                         "sources": ["ulysses_sequence_gb300/csrc/attn_bwd.cu", "ulysses_sequence_gb300/csrc/common.cuh"]},
-    "attn_fwd_kernel": {"bytes": 1060227840, "workload": "gpt7b", "sha": "d021cdfa8a93b09a",
+    "attn_fwd_kernel": {"bytes": 1059226368, "workload": "gpt7b", "sha": "9da78dea16979901",
                         "sources": ["ulysses_sequence_gb300/csrc/attn_fwd.cu", "ulysses_sequence_gb300/csrc/common.cuh"]},
 }
 
@@ -421,6 +421,38 @@ def main():
     out_flops = 2 * rows * hidden * w.H * w.d
     del xs, w_qkv, w_o, pq, pk, pv, py
 
+    # ---- the Ulysses-ring hybrid on the same tensors: P = 2H shards (beyond the head cut's
+    # P <= H) as P_ring = 2 ring blocks of P_u = H shards; the same attention, so the same flops
+    usp = None
+    if w.mask in ("causal", "none") and (w.Hkv % w.H == 0 or w.H % w.Hkv == 0):
+        P_ring, P_usp = 2, 2 * w.H
+        Pu = P_usp // P_ring
+        if w.L % P_usp == 0 and (w.L // P_usp) % 8 == 0 and (Pu % w.Hkv == 0 or w.Hkv % Pu == 0):
+            # the token-sharded bytes of P shards are those of any other shard count: re-view them
+            uq, uk, uv, udo = (x[n].reshape(P_usp, w.B, w.L // P_usp, x[n].shape[3], w.d)
+                               for n in ("q", "k", "v", "do"))
+            uo = torch.empty_like(uq)
+            ulse = torch.empty((P_ring, Pu, w.B, w.H // Pu, w.L // P_ring), dtype=torch.float32, device=dev)
+            udq, udk, udv = torch.empty_like(uq), torch.empty_like(uk), torch.empty_like(uv)
+            uws = U.usp_workspace(uq, P_usp, P_ring, w.Hkv)
+            ufwd = lambda: U.usp_attn_fwd(uq, uk, uv, P_usp, P_ring, mask, o=uo, lse=ulse, workspace=uws)  # noqa: E731
+            ubwd = lambda: U.usp_attn_bwd(uq, uk, uv, uo, ulse, udo, P_usp, P_ring, mask, dq=udq, dk=udk,  # noqa: E731
+                                          dv=udv, workspace=uws)
+            for _ in range(3):
+                ufwd()
+                ubwd()
+            ufwd_ms = cuda_events_time(ufwd, stream, 5)
+            ubwd_ms = cuda_events_time(ubwd, stream, 5)
+            pairs_fwd = 3 if w.mask == "causal" else 4
+            usp = {"P": P_usp, "P_ring": P_ring, "P_u": Pu, "fwd_ms": ufwd_ms, "bwd_ms": ubwd_ms,
+                   "fwd_tflops": f_fwd / (ufwd_ms * 1e-3) / 1e12,
+                   "bwd_tflops": f_bwd / (ubwd_ms * 1e-3) / 1e12 if w.backward else None,
+                   "fwd_bwd_tflops": (f_fwd + f_bwd) / ((ufwd_ms + ubwd_ms) * 1e-3) / 1e12,
+                   "launches_per_step": pairs_fwd + P_ring + pairs_fwd * 6,
+                   "note": "same tensors and mask, P > H; block-pair attention + merge (fwd), "
+                           "block-pair backward + fp32 gradient sums (bwd); not part of the step"}
+            del uo, ulse, udq, udk, udv, uws
+
     # ---- dominant launch group: the backward call (Delta prep + main + dQ convert)
     bwd_avg = statistics.mean(bwd_ms) if w.backward else 0.0
     fwd_avg = statistics.mean(fwd_ms)
@@ -477,6 +509,7 @@ def main():
                             "qkv_frac": qkv_flops / (qkv_ms * 1e-3) / 1e12 / peak_tf,
                             "out_frac": out_flops / (out_ms * 1e-3) / 1e12 / peak_tf,
                             "note": "x [B*L][H*d_h] -> Q, K, V token-sharded; O -> y; not part of the step"},
+            "usp": usp,
             "accounted_alltoall_bytes_per_rank": {"fwd": comm, "leaves_rank": comm * (w.P - 1) // w.P,
                                                   "note": "4Nh/P in bf16 bytes, accounted, not measured over a link"},
             "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak_tf,
