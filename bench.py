@@ -44,9 +44,9 @@ METRIC = "Ulysses attn fwd+bwd TFLOP/s & % BF16 peak; relayout HBM GB/s"
 # profiles/attn_kernels_gpt7b.md. A figure is reported only while the kernel sources still
 # hash to the value recorded with it; after any change it reads as null until re-captured.
 NCU_TRAFFIC = {
-    "attn_bwd_kernel": {"bytes": 2645222912, "workload": "gpt7b", "sha": "bd7b9efb74ce932f",
+    "attn_bwd_kernel": {"bytes": 2648437248, "workload": "gpt7b", "sha": "6e042577d3a8153d",
                         "sources": ["ulysses_sequence_gb300/csrc/attn_bwd.cu", "ulysses_sequence_gb300/csrc/common.cuh"]},
-    "attn_fwd_kernel": {"bytes": 1059226368, "workload": "gpt7b", "sha": "9da78dea16979901",
+    "attn_fwd_kernel": {"bytes": 1060419328, "workload": "gpt7b", "sha": "9da78dea16979901",
                         "sources": ["ulysses_sequence_gb300/csrc/attn_fwd.cu", "ulysses_sequence_gb300/csrc/common.cuh"]},
 }
 
@@ -448,7 +448,9 @@ def main():
                    "fwd_tflops": f_fwd / (ufwd_ms * 1e-3) / 1e12,
                    "bwd_tflops": f_bwd / (ubwd_ms * 1e-3) / 1e12 if w.backward else None,
                    "fwd_bwd_tflops": (f_fwd + f_bwd) / ((ufwd_ms + ubwd_ms) * 1e-3) / 1e12,
-                   "launches_per_step": pairs_fwd + P_ring + pairs_fwd * 6,
+                   # fwd: one attention per block pair + one merge per query block; bwd: one
+                   # backward per pair + Delta prep and dQ conversion per query block
+                   "launches_per_step": 2 * pairs_fwd + 3 * P_ring,
                    "note": "same tensors and mask, P > H; block-pair attention + merge (fwd), "
                            "block-pair backward + fp32 gradient sums (bwd); not part of the step"}
             del uo, ulse, udq, udk, udv, uws

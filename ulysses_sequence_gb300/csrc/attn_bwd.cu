@@ -25,6 +25,8 @@
 //      1 MMA issuer, 2-9 softmax / dS / dQ drain, two warps per tensor-memory lane
 //      quadrant, each taking 64 of the step's 128 queries.
 //   3. bwd_dq_convert: dQ = bf16(scale * accumulator) into the output layout.
+#include <type_traits>
+
 #include "common.cuh"
 #include "ulysses_internal.h"
 
@@ -50,6 +52,16 @@ struct BwdParams {
     const int32_t* qrows;
     uint32_t* err;
 };
+
+// The accumulating kernels' parameters (a separate type: growing BwdParams itself measurably
+// slowed the plain kernel)
+struct BwdAccParams : BwdParams {
+    float* dk_acc;   // fp32 accumulators of dK, dV (layout of dK)
+    float* dv_acc;
+    int dkv_mode;    // 1 fp32 store, 2 fp32 add, 3 bf16(accumulator + part)
+};
+template <bool ACC>
+using BwdParamsOf = typename std::conditional<ACC, BwdAccParams, BwdParams>::type;
 
 template <int D>
 struct BwdCfg {
@@ -199,11 +211,12 @@ __device__ __forceinline__ int bwd_q_step(const BwdParams& p, int first, int it)
 // queries) of an MMA reading them as its A operand therefore starts at column a_col(k).
 __device__ __forceinline__ uint32_t a_col(int k) { return uint32_t(8 * k + (k >= 4 ? 64 : 0)); }
 
-template <int D, int MASK>
+// ACC: dK, dV go through the fp32 accumulators (dkv_mode 1-3) instead of straight to bf16
+template <int D, int MASK, bool ACC>
 __global__ void __launch_bounds__(320, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const BwdParams p) {
+                const BwdParamsOf<ACC> p) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -548,7 +561,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // half 0 writes dV, half 1 writes dK
             const uint32_t tcol = hf == 0 ? C::T_DV : C::T_DK;
             const float mul = hf == 0 ? 1.0f : p.scale;
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(hf == 0 ? p.dv : p.dk) + kv_row_offset(p, key, u, D);
+            const size_t koff = kv_row_offset(p, key, u, D);
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(hf == 0 ? p.dv : p.dk) + koff;
             const bool valid = key < p.L;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -559,6 +573,22 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[i] = (n_it > 0) ? x[i] * mul : 0.f;
+                if constexpr (ACC) {
+                    if (!valid) continue;
+                    float4* a4 = reinterpret_cast<float4*>((hf == 0 ? p.dv_acc : p.dk_acc) + koff + c * 32);
+                    if (p.dkv_mode >= 2) {
+#pragma unroll
+                        for (int y = 0; y < 8; ++y) {
+                            const float4 t = a4[y];
+                            x[4 * y] += t.x; x[4 * y + 1] += t.y; x[4 * y + 2] += t.z; x[4 * y + 3] += t.w;
+                        }
+                    }
+                    if (p.dkv_mode <= 2) {
+#pragma unroll
+                        for (int y = 0; y < 8; ++y) a4[y] = make_float4(x[4 * y], x[4 * y + 1], x[4 * y + 2], x[4 * y + 3]);
+                        continue;
+                    }
+                }
                 if (valid) {
                     uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
@@ -666,11 +696,11 @@ size_t bwd_workspace_bytes(const ulysses_shape_t& s) {
     return acc_bytes(s) + (rows * 4 + 255) / 256 * 256;
 }
 
-template <int D, int MASK>
+template <int D, int MASK, bool ACC>
 static int launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
-                        const BwdParams& p, cudaStream_t stream) {
+                        const BwdParamsOf<ACC>& p, cudaStream_t stream) {
     using C = BwdCfg<D>;
-    auto kern = attn_bwd_kernel<D, MASK>;
+    auto kern = attn_bwd_kernel<D, MASK, ACC>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -688,7 +718,8 @@ static int launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
 
 template <int D>
 static int launch_bwd_d(const ulysses_shape_t& s, const MaskArgs& m, BwdParams& p, const void* q, const void* k,
-                        const void* v, const void* o, const void* dO, void* dq, cudaStream_t stream) {
+                        const void* v, const void* o, const void* dO, void* dq, const BwdChain& chain,
+                        cudaStream_t stream) {
     CUtensorMap mq, mk, mv, mdo;
     if (!encode_qkv_map(&mq, q, s, p.layout, p.box_rows, s.H, s.H / s.P) ||
         !encode_qkv_map(&mdo, dO, s, p.layout, p.box_rows, s.H, s.H / s.P) ||
@@ -699,22 +730,35 @@ static int launch_bwd_d(const ulysses_shape_t& s, const MaskArgs& m, BwdParams& 
     const size_t rows = size_t(s.B) * s.H * s.L;
     size_t blocks = (rows * 8 + 255) / 256;
     if (blocks > size_t(sms) * 16) blocks = size_t(sms) * 16;
-    bwd_prep_kernel<D><<<unsigned(blocks), 256, 0, stream>>>(p, static_cast<const __nv_bfloat16*>(o),
-                                                              static_cast<const __nv_bfloat16*>(dO),
-                                                              const_cast<float*>(p.delta));
-    if (cudaGetLastError() != cudaSuccess) return ULYSSES_ERR_CUDA;
+    if (chain.prep) {
+        bwd_prep_kernel<D><<<unsigned(blocks), 256, 0, stream>>>(p, static_cast<const __nv_bfloat16*>(o),
+                                                                  static_cast<const __nv_bfloat16*>(dO),
+                                                                  const_cast<float*>(p.delta));
+        if (cudaGetLastError() != cudaSuccess) return ULYSSES_ERR_CUDA;
+    }
     int rc;
-    if (m.kind == ULYSSES_MASK_CAUSAL) rc = launch_bwd_t<D, ULYSSES_MASK_CAUSAL>(mq, mk, mv, mdo, p, stream);
-    else if (m.kind == ULYSSES_MASK_NONE) rc = launch_bwd_t<D, ULYSSES_MASK_NONE>(mq, mk, mv, mdo, p, stream);
-    else rc = launch_bwd_t<D, ULYSSES_MASK_BLOCK_SPARSE>(mq, mk, mv, mdo, p, stream);
+    if (chain.dkv_mode != 0) {
+        BwdAccParams ap;
+        static_cast<BwdParams&>(ap) = p;
+        ap.dk_acc = chain.dk_acc;
+        ap.dv_acc = chain.dv_acc;
+        ap.dkv_mode = chain.dkv_mode;
+        // the accumulating epilogue is built for the masks of the ring blocks only
+        if (m.kind == ULYSSES_MASK_CAUSAL) rc = launch_bwd_t<D, ULYSSES_MASK_CAUSAL, true>(mq, mk, mv, mdo, ap, stream);
+        else if (m.kind == ULYSSES_MASK_NONE) rc = launch_bwd_t<D, ULYSSES_MASK_NONE, true>(mq, mk, mv, mdo, ap, stream);
+        else return ULYSSES_ERR_UNSUPPORTED;
+    } else if (m.kind == ULYSSES_MASK_CAUSAL) rc = launch_bwd_t<D, ULYSSES_MASK_CAUSAL, false>(mq, mk, mv, mdo, p, stream);
+    else if (m.kind == ULYSSES_MASK_NONE) rc = launch_bwd_t<D, ULYSSES_MASK_NONE, false>(mq, mk, mv, mdo, p, stream);
+    else rc = launch_bwd_t<D, ULYSSES_MASK_BLOCK_SPARSE, false>(mq, mk, mv, mdo, p, stream);
     if (rc != ULYSSES_OK) return rc;
+    if (!chain.convert) return ULYSSES_OK;
     bwd_dq_convert_kernel<D><<<unsigned(blocks), 256, 0, stream>>>(p, static_cast<__nv_bfloat16*>(dq));
     return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }
 
 int launch_attn_bwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, int layout, const void* q,
                     const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
-                    void* dk, void* dv, void* workspace, cudaStream_t stream) {
+                    void* dk, void* dv, void* workspace, cudaStream_t stream, const BwdChain& chain) {
     BwdParams p{};
     p.B = s.B; p.L = s.L; p.H = s.H; p.P = s.P; p.Hp = s.H / s.P; p.Lp = s.L / s.P;
     const KvInfo kv = kv_info(s);
@@ -729,12 +773,14 @@ int launch_attn_bwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, in
     p.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes(s));
     p.dk = dk;
     p.dv = dv;
+    if (chain.dkv_mode < 0 || chain.dkv_mode > 3 || (chain.dkv_mode != 0 && (!chain.dk_acc || !chain.dv_acc)))
+        return ULYSSES_ERR_INVALID_ARG;
     p.colptr = m.k_colptr;
     p.qrows = m.k_qrows;
     p.err = device_error_word();
     if (!p.err) return ULYSSES_ERR_CUDA;
-    if (s.d_h == 128) return launch_bwd_d<128>(s, m, p, q, k, v, o, dO, dq, stream);
-    return launch_bwd_d<64>(s, m, p, q, k, v, o, dO, dq, stream);
+    if (s.d_h == 128) return launch_bwd_d<128>(s, m, p, q, k, v, o, dO, dq, chain, stream);
+    return launch_bwd_d<64>(s, m, p, q, k, v, o, dO, dq, chain, stream);
 }
 
 }  // namespace ulysses

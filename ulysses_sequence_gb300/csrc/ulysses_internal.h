@@ -60,9 +60,21 @@ int launch_kv_replicated(const ulysses_shape_t& s, const void* in, void* out, cu
 int launch_attn_fwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, int layout, const void* q,
                     const void* k, const void* v, void* o, float* lse, cudaStream_t stream);
 
+// How one backward launch joins a chain of launches that add into the same gradients (the block
+// pairs of the Ulysses-ring hybrid). The default is a standalone backward.
+struct BwdChain {
+    bool prep = true;     // compute Delta and zero the fp32 dQ accumulator (a query block's first launch)
+    bool convert = true;  // write dQ from the accumulator (a query block's last launch)
+    // dK, dV: 0 stored bf16; 1 stored fp32 to the accumulators; 2 added into them;
+    // 3 stored bf16(accumulator + this launch's part)
+    int dkv_mode = 0;
+    float* dk_acc = nullptr;  // same layout as dK, fp32
+    float* dv_acc = nullptr;
+};
+
 int launch_attn_bwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, int layout, const void* q,
                     const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
-                    void* dk, void* dv, void* workspace, cudaStream_t stream);
+                    void* dk, void* dv, void* workspace, cudaStream_t stream, const BwdChain& chain = BwdChain());
 
 size_t bwd_workspace_bytes(const ulysses_shape_t& s);
 

@@ -8,7 +8,8 @@
 // The block-pair attentions are the library's own forward and backward on tensor slices:
 // causal on the diagonal block pair, every pair below it (or all pairs for a dense mask). The
 // backward of a block pair uses the merged O and lse, so its probabilities are those of the
-// whole row; its partial gradients are summed over block pairs in fp32.
+// whole row; its partial gradients are summed over block pairs in fp32 inside the block-pair
+// backward (its dQ accumulator, and an fp32 store/add mode of its dK, dV epilogue).
 #include "common.cuh"
 #include "ulysses_internal.h"
 
@@ -78,29 +79,6 @@ __global__ void __launch_bounds__(256) usp_merge_kernel(MergeArgs a) {
     }
 }
 
-// acc[i] (fp32) += part[i] (bf16), or (final) out[i] = bf16(acc[i] + part[i]); n a multiple of 8.
-__global__ void __launch_bounds__(256) usp_accumulate_kernel(float* acc, const __nv_bfloat16* part, size_t n8,
-                                                             __nv_bfloat16* out) {
-    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += size_t(gridDim.x) * blockDim.x) {
-        const uint4 x = reinterpret_cast<const uint4*>(part)[i];
-        const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&x);
-        float4* a4 = reinterpret_cast<float4*>(acc) + 2 * i;
-        float4 lo = a4[0], hi = a4[1];
-        float2 f;
-        f = __bfloat1622float2(x2[0]); lo.x += f.x; lo.y += f.y;
-        f = __bfloat1622float2(x2[1]); lo.z += f.x; lo.w += f.y;
-        f = __bfloat1622float2(x2[2]); hi.x += f.x; hi.y += f.y;
-        f = __bfloat1622float2(x2[3]); hi.z += f.x; hi.w += f.y;
-        if (out) {
-            reinterpret_cast<uint4*>(out)[i] = make_uint4(pack_bf16(lo.x, lo.y), pack_bf16(lo.z, lo.w),
-                                                          pack_bf16(hi.x, hi.y), pack_bf16(hi.z, hi.w));
-        } else {
-            a4[0] = lo;
-            a4[1] = hi;
-        }
-    }
-}
-
 namespace {
 
 unsigned grid_for(size_t work, int per_block) {
@@ -138,11 +116,9 @@ size_t usp_workspace_bytes(const ulysses_shape_t& s, int P_ring) {
     const UspGeom g = usp_geom(s, P_ring);
     // forward: up to P_ring partial (O, lse) of one query block
     const size_t fwd = size_t(P_ring) * (g.part_bytes + g.lse_bytes);
-    // backward: fp32 sums of dQ, dK, dV over the whole sequence, one block pair's bf16 partials,
-    // and the block-pair backward's own workspace
-    const size_t kv_part = align256(g.kv_elems * 2);
-    const size_t bwd = align256(size_t(P_ring) * g.q_elems * 4) + 2 * align256(size_t(P_ring) * g.kv_elems * 4) +
-                       g.part_bytes + 2 * kv_part + bwd_workspace_bytes(g.sub);
+    // backward: fp32 sums of dK and dV over the whole sequence, and the block-pair backward's
+    // own workspace (whose fp32 dQ accumulator carries a query block across its pairs)
+    const size_t bwd = 2 * align256(size_t(P_ring) * g.kv_elems * 4) + bwd_workspace_bytes(g.sub);
     return fwd > bwd ? fwd : bwd;
 }
 
@@ -189,23 +165,11 @@ int launch_usp_bwd(const ulysses_shape_t& s, int P_ring, const MaskArgs& m, floa
                    void* ws, cudaStream_t stream) {
     const UspGeom g = usp_geom(s, P_ring);
     char* w = static_cast<char*>(ws);
-    float* acc_q = reinterpret_cast<float*>(w);
-    w += align256(size_t(P_ring) * g.q_elems * 4);
     float* acc_k = reinterpret_cast<float*>(w);
     w += align256(size_t(P_ring) * g.kv_elems * 4);
     float* acc_v = reinterpret_cast<float*>(w);
     w += align256(size_t(P_ring) * g.kv_elems * 4);
-    __nv_bfloat16* pq = reinterpret_cast<__nv_bfloat16*>(w);
-    w += g.part_bytes;
-    __nv_bfloat16* pk = reinterpret_cast<__nv_bfloat16*>(w);
-    w += align256(g.kv_elems * 2);
-    __nv_bfloat16* pv = reinterpret_cast<__nv_bfloat16*>(w);
-    w += align256(g.kv_elems * 2);
     void* sub_ws = w;
-    if (cudaMemsetAsync(acc_q, 0, size_t(P_ring) * g.q_elems * 4, stream) != cudaSuccess ||
-        cudaMemsetAsync(acc_k, 0, size_t(P_ring) * g.kv_elems * 4, stream) != cudaSuccess ||
-        cudaMemsetAsync(acc_v, 0, size_t(P_ring) * g.kv_elems * 4, stream) != cudaSuccess)
-        return ULYSSES_ERR_CUDA;
     const bool causal = m.kind == ULYSSES_MASK_CAUSAL;
     MaskArgs none{ULYSSES_MASK_NONE, nullptr, nullptr, nullptr, nullptr};
     const __nv_bfloat16* q16 = static_cast<const __nv_bfloat16*>(q);
@@ -213,26 +177,32 @@ int launch_usp_bwd(const ulysses_shape_t& s, int P_ring, const MaskArgs& m, floa
     const __nv_bfloat16* v16 = static_cast<const __nv_bfloat16*>(v);
     const __nv_bfloat16* o16 = static_cast<const __nv_bfloat16*>(o);
     const __nv_bfloat16* do16 = static_cast<const __nv_bfloat16*>(dO);
-    // number of block pairs each query block / key block takes part in (the last one writes bf16)
+    __nv_bfloat16* dq16 = static_cast<__nv_bfloat16*>(dq);
+    __nv_bfloat16* dk16 = static_cast<__nv_bfloat16*>(dk);
+    __nv_bfloat16* dv16 = static_cast<__nv_bfloat16*>(dv);
+    // block pairs each query block / key block takes part in
     auto q_pairs = [&](int i) { return causal ? i + 1 : P_ring; };
     auto k_pairs = [&](int j) { return causal ? P_ring - j : P_ring; };
     int seen_k[kMaxRing] = {};
+    // Query blocks outer, key blocks inner: a query block's pairs run back to back, so its dQ
+    // stays in the block-pair backward's fp32 accumulator from the first pair (which zeroes it
+    // and computes Delta) to the last (which writes bf16 dQ). dK, dV of a key block are spread
+    // over query blocks: its first pair stores them fp32, later pairs add, the last rounds.
     for (int i = 0; i < P_ring; ++i) {
         for (int j = 0; j < q_pairs(i); ++j) {
             const MaskArgs& mj = (causal && j == i) ? m : none;
+            BwdChain ch;
+            ch.prep = j == 0;
+            ch.convert = j + 1 == q_pairs(i);
+            const int nk = k_pairs(j), c = seen_k[j]++;
+            ch.dkv_mode = nk == 1 ? 0 : (c == 0 ? 1 : (c + 1 == nk ? 3 : 2));
+            ch.dk_acc = acc_k + j * g.kv_elems;
+            ch.dv_acc = acc_v + j * g.kv_elems;
             int rc = launch_attn_bwd(g.sub, mj, scale, ULYSSES_LAYOUT_TOKEN_SHARDED, q16 + i * g.q_elems,
                                      k16 + j * g.kv_elems, v16 + j * g.kv_elems, o16 + i * g.q_elems,
-                                     lse + i * g.lse_elems, do16 + i * g.q_elems, pq, pk, pv, sub_ws, stream);
+                                     lse + i * g.lse_elems, do16 + i * g.q_elems, dq16 + i * g.q_elems,
+                                     dk16 + j * g.kv_elems, dv16 + j * g.kv_elems, sub_ws, stream, ch);
             if (rc != ULYSSES_OK) return rc;
-            const bool last_q = j + 1 == q_pairs(i);
-            const bool last_k = ++seen_k[j] == k_pairs(j);
-            usp_accumulate_kernel<<<grid_for(g.q_elems / 8, 256), 256, 0, stream>>>(
-                acc_q + i * g.q_elems, pq, g.q_elems / 8, last_q ? static_cast<__nv_bfloat16*>(dq) + i * g.q_elems : nullptr);
-            usp_accumulate_kernel<<<grid_for(g.kv_elems / 8, 256), 256, 0, stream>>>(
-                acc_k + j * g.kv_elems, pk, g.kv_elems / 8, last_k ? static_cast<__nv_bfloat16*>(dk) + j * g.kv_elems : nullptr);
-            usp_accumulate_kernel<<<grid_for(g.kv_elems / 8, 256), 256, 0, stream>>>(
-                acc_v + j * g.kv_elems, pv, g.kv_elems / 8, last_k ? static_cast<__nv_bfloat16*>(dv) + j * g.kv_elems : nullptr);
-            if (cudaGetLastError() != cudaSuccess) return ULYSSES_ERR_CUDA;
         }
     }
     return ULYSSES_OK;
