@@ -8,6 +8,8 @@ P > H (the case the hybrid exists for), pure ring (P_u = 1), grouped key/value h
 a ragged tail inside each ring block, and P_ring = 1 equal to the plain Ulysses calls.
 """
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -15,7 +17,7 @@ import torch
 import oracle
 import ulysses_sequence_gb300 as U
 import workloads
-from gpu_util import ErrStats, LSE_MAX_ABS, need_gpu
+from gpu_util import ErrStats, LSE_MAX_ABS, env_rows, need_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -122,3 +124,56 @@ def test_usp_rejects_bad_splits():
         U.usp_attn_fwd(q, q, q, 8, 3, mask)   # P_ring does not divide P
     assert U.ulysses_usp_workspace_size(U.Shape(1, 512, 4, 128, 8, 0), 3) == 0
     assert U.ulysses_usp_workspace_size(U.Shape(1, 512, 4, 128, 8, 0), 2) > 0
+
+
+def test_usp_gpt7b_sampled_rows():
+    """The configuration the benchmark times: the GPT-7B-like layer (B=1, L=32768, H=32,
+    d_h=128, causal) re-viewed as P = 64 = 2H token shards, P_ring = 2. 4096 seeded query rows
+    of 8 heads against the oracle's whole-sequence attention: O, lse and dQ of those rows from a
+    pass with the full dO (run A); dK, dV over every key from a pass whose dO is zero outside
+    those rows (run B), which then hold exactly the sampled rows' contributions."""
+    w = workloads.WORKLOADS["gpt7b"]
+    P_ring, P = 2, 2 * w.H
+    B, L, H, d = w.B, w.L, w.H, w.d
+    heads = (0, 4, 9, 13, 18, 22, 27, 31)
+    t = workloads.draw_workload(w)
+    rows = workloads.sample_rows(B, L, env_rows(w.sampled_rows), seed=w.seed)
+    keep = torch.zeros((B, L), dtype=torch.bool)
+    keep[torch.from_numpy(rows[:, 0]), torch.from_numpy(rows[:, 1])] = True
+    # the same bytes as P token shards: [P][B][L/P][H][d]
+    dev = {n: x.cuda().reshape(P, B, L // P, x.shape[3], d) for n, x in t.items()}
+    keep_tok = keep.reshape(B, P, L // P).permute(1, 0, 2)[..., None, None].cuda().to(torch.bfloat16)
+    mask = U.Mask.causal()
+    o, lse = U.usp_attn_fwd(dev["q"], dev["k"], dev["v"], P, P_ring, mask)
+    dqA, _, _ = U.usp_attn_bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], P, P_ring, mask)
+    do_b = dev["do"] * keep_tok
+    dqB, dkB, dvB = U.usp_attn_bwd(dev["q"], dev["k"], dev["v"], o, lse, do_b, P, P_ring, mask)
+    torch.cuda.synchronize()
+    st, word = U.device_status()
+    assert st == U.OK, hex(word)
+
+    def logical_t(x):
+        return x.cpu().permute(1, 0, 2, 3, 4).reshape(B, L, x.shape[3], d)
+
+    O, dQA, dQB, dKB, dVB = (logical_t(x) for x in (o, dqA, dqB, dkB, dvB))
+    LSE = torch.from_numpy(_usp_lse_logical(lse.cpu().double().numpy()))
+    assert torch.count_nonzero(dQB.float()[~keep]) == 0
+    del dev, o, dqA, dqB, dkB, dvB, do_b
+    torch.cuda.empty_cache()
+
+    stats = {n: ErrStats(n) for n in ("o", "dq", "dk", "dv")}
+    lse_err = 0.0
+    bits = {n: workloads.to_bf16_bits(x) for n, x in t.items()}
+    workers = min(8, os.cpu_count() or 1)
+    # whole-sequence attention: any shard count of the oracle's relayout gives it; use the layer's own
+    for res in oracle.attention_sampled(bits["q"], bits["k"], bits["v"], bits["do"], w.P, oracle.Mask("causal"),
+                                        rows, heads=heads, workers=workers):
+        b, h, r = res["b"], res["h"], torch.from_numpy(res["rows"])
+        stats["o"].add(O[b, r, h].double().numpy(), res["o"])
+        stats["dq"].add(dQA[b, r, h].double().numpy(), res["dq"])
+        stats["dk"].add(dKB[b, :, h].double().numpy(), res["dk"])
+        stats["dv"].add(dVB[b, :, h].double().numpy(), res["dv"])
+        lse_err = max(lse_err, float(np.abs(LSE[b, h, r].numpy() - res["lse"]).max()))
+    for s in stats.values():
+        s.check()
+    assert lse_err <= LSE_MAX_ABS, lse_err
