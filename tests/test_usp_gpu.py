@@ -4,8 +4,9 @@ P = P_u * P_ring token shards: ring blocks of L / P_ring tokens, each spread ove
 groups by the Ulysses relayout, per-block-pair attention merged by the online-softmax rule.
 Whatever the split, the result is exact attention over the whole sequence, so the oracle is
 attention over all L tokens at once (one shard). Checked on every row: causal and dense masks,
-P > H (the case the hybrid exists for), pure ring (P_u = 1), grouped key/value heads, d_h 64,
-a ragged tail inside each ring block, and P_ring = 1 equal to the plain Ulysses calls.
+P > H (the case the hybrid exists for), pure ring (P_u = 1), grouped key/value heads (whole
+heads and copies per head group), d_h 64, a ragged tail inside each ring block, and
+P_ring = 1 equal to the plain Ulysses calls; and at the benchmarked size on sampled rows.
 """
 
 import os
@@ -87,6 +88,8 @@ CASES = [
     ("dense_gqa_d64_b2", 2, 384, 8, 2, 64, 4, 4, "none"),
     ("ragged_block_gqa", 1, 640, 8, 4, 128, 4, 2, "causal"),
     ("dense_ring3", 1, 768, 4, 4, 128, 6, 3, "none"),
+    # P_u = 4 > H_kv = 2: each head group of a ring block gets a copy of one key/value head
+    ("kv_copies_p8_ring2", 1, 512, 8, 2, 128, 8, 2, "causal"),
 ]
 
 
