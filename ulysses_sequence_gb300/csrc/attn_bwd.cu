@@ -18,12 +18,15 @@
 //        dQ^T = K^T dS^T  (M=d, N=128, K=128)   dS^T also in shared memory (B operand);
 //                                               written over dP^T once dK has read dS^T,
 //                                               then added into the fp32 accumulator by
-//                                               coalesced reductions from registers
+//                                               coalesced 128-byte reductions, half of
+//                                               them from the softmax warps' registers,
+//                                               half staged for two drain warps
 //      The next step's S^T is issued right after dV, so the exponentials of the next P
 //      overlap dK and dQ^T on the tensor cores.
 //      Warps: 0 TMA producer (K, V once; per step Q into one of two slots, dO into one),
-//      1 MMA issuer, 2-9 softmax / dS / dQ drain, two warps per tensor-memory lane
-//      quadrant, each taking 64 of the step's 128 queries.
+//      1 MMA issuer, 2-9 softmax / dS / dQ^T read-out, two warps per tensor-memory lane
+//      quadrant, each taking 64 of the step's 128 queries, 10-11 dQ drain. Twelve warps
+//      keep 168 registers per thread (three per sub-partition, as ten already put on two).
 //   3. bwd_dq_convert: dQ = bf16(scale * accumulator) into the output layout.
 #include <type_traits>
 
@@ -75,8 +78,16 @@ struct BwdCfg {
     static constexpr uint32_t DST_BYTES = kTile * kQStep * 2;
     static constexpr uint32_t OFF_LSE = OFF_DST + DST_BYTES;    // [2][128] fp32
     static constexpr uint32_t OFF_DELTA = OFF_LSE + 2 * kQStep * 4;  // [2][128] fp32
-    static constexpr uint32_t OFF_BAR = OFF_DELTA + 2 * kQStep * 4;
-    static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
+    // staging of the softmax warps' dQ^T rows for the drain warps: 32 queries x 32 features
+    // fp32 (4 KB) per softmax warp
+    static constexpr uint32_t OFF_STG = OFF_DELTA + 2 * kQStep * 4;
+    static constexpr uint32_t STG_BYTES = 8 * 4096;
+    static constexpr uint32_t OFF_BAR = OFF_STG + STG_BYTES;
+    // 1 KB of slack to align the dynamic shared memory base where it fits; without it the
+    // kernel checks that the base is 1024-byte aligned (it is, after the 1 KB the system keeps)
+    static constexpr uint32_t SLACK = OFF_BAR + 256 + 1024 <= 232448 ? 1024 : 0;
+    static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + SLACK;
+    static constexpr int NQ = D / 32 < 4 ? D / 32 : 4;  // lane quadrants that hold dQ^T rows
     static constexpr uint32_t TMEM_COLS = 512;
     // tensor-memory columns: S^T (then P^T), dP^T (then dS^T, then dQ^T), dV, dK
     static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
@@ -212,13 +223,25 @@ __device__ __forceinline__ int bwd_q_step(const BwdParams& p, int first, int it)
 __device__ __forceinline__ uint32_t a_col(int k) { return uint32_t(8 * k + (k >= 4 ? 64 : 0)); }
 
 // ACC: dK, dV go through the fp32 accumulators (dkv_mode 1-3) instead of straight to bf16
+// Whether the kernel has the two dQ drain warps: the block-sparse variant keeps every reduction
+// in the softmax warps (with the drain its softmax loop spills registers, and measured slower).
+template <int MASK>
+constexpr bool bwd_has_drain() { return MASK != ULYSSES_MASK_BLOCK_SPARSE; }
+template <int MASK>
+constexpr int bwd_threads() { return bwd_has_drain<MASK>() ? 384 : 320; }
+
 template <int D, int MASK, bool ACC>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(bwd_threads<MASK>(), 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const BwdParamsOf<ACC> p) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
+    if (C::SLACK == 0 && (smem_u32(smem_raw) & 1023u) != 0) {
+        // uniform early exit, before any barrier or tensor memory exists
+        if (threadIdx.x == 0) record_error(p.err, (KID_BWD << 24) | (ROLE_LOAD << 16) | 0xa1u);
+        return;
+    }
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sK = smem + C::OFF_K;
     uint8_t* sV = smem + C::OFF_V;
@@ -241,7 +264,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint64_t* dq_free = bars + 12;    // 8 warps
     uint64_t* dkdv_done = bars + 13;
     uint64_t* drain = bars + 14;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+    uint64_t* stg_full = bars + 15;   // softmax warps holding dQ^T rows: rows staged
+    uint64_t* stg_free = bars + 16;   // 2 drain warps: staging slots read out
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = static_cast<int>(warp_id());
@@ -271,6 +296,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(dq_free, 8);
         mbar_init(dkdv_done, 1);
         mbar_init(drain, 1);
+        mbar_init(stg_full, 2 * C::NQ);
+        mbar_init(stg_free, 2);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -434,7 +461,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_drain(drain, 0);
             }
         }
-    } else {
+    } else if (warp < 10) {
         // ------------------------------------------------------------------ softmax, dS, dQ
         // thread = one key (tensor-memory lane); half hf takes queries [64 hf, 64 hf + 64)
         const int wq = warp & 3;
@@ -545,13 +572,34 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dq_free);
-            if (dq_lanes) {
+            if (dq_lanes && !bwd_has_drain<MASK>()) {
                 // one coalesced 128-byte reduction per query: the warp's 32 lanes are 32
                 // consecutive features of that query's row of the accumulator
                 float* dst = p.dq_acc + (size_t(b * p.H + h) * p.n_tiles * kTile + qstep * kQStep + 64 * hf) * D +
                              wq * 32 + lane;
 #pragma unroll
                 for (int c = 0; c < 64; ++c) red_add_f32(dst + c * D, v[c]);
+            } else if (dq_lanes) {
+                // The warp's rows of dQ^T: 64 queries x 32 features. Queries [32, 64) are staged
+                // for the drain warps (row = query, lane = feature: each store is one
+                // conflict-free 128-byte row); queries [0, 32) are added here, one coalesced
+                // 128-byte reduction per query. Splitting the reductions between the two groups
+                // of warps takes half of their issue time off this loop, whose length sets
+                // the step (reductions issue faster from more warps, so the drain warps cannot
+                // take them all).
+                if (it > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(stg_free, (it - 1) & 1, ab, ROLE_DQ, 2));
+                    if (!ok) break;
+                }
+                float* r2 = reinterpret_cast<float*>(smem + C::OFF_STG + (hf * 4 + wq) * 4096);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) r2[c * 32 + lane] = v[32 + c];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(stg_full);
+                float* dst = p.dq_acc + (size_t(b * p.H + h) * p.n_tiles * kTile + qstep * kQStep + 64 * hf) * D +
+                             wq * 32 + lane;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) red_add_f32(dst + c * D, v[c]);
             }
         }
         // ------------------------------------------------------------------ dK, dV epilogue
@@ -597,6 +645,33 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                            pack_bf16(x[8 * y + 4], x[8 * y + 5]), pack_bf16(x[8 * y + 6], x[8 * y + 7]));
                 }
             }
+        }
+    } else {
+        // ------------------------------------------------------------------ dQ drain (warps 10, 11)
+        // Drain warp dw adds the rows staged by the softmax warps of query half dw (queries
+        // 64 dw + [32, 64), every feature quadrant) into the fp32 accumulator: each row is
+        // loaded from shared memory first, then added by one coalesced 128-byte reduction.
+        const int dw = warp - 10;
+        bool ok = true;
+        for (int it = 0; ok && it < n_it; ++it) {
+            const int ih = it / n_per;
+            const int h = u.h_first + ih;
+            const int qstep = bwd_q_step<MASK>(p, q_first, it - ih * n_per);
+            ok = __all_sync(0xffffffffu, mbar_wait(stg_full, it & 1, ab, ROLE_DQ, 3));
+            if (!ok) break;
+            const size_t row0 = size_t(b * p.H + h) * p.n_tiles * kTile + size_t(qstep) * kQStep + 64 * dw;
+#pragma unroll 1
+            for (int wq = 0; wq < C::NQ; ++wq) {
+                const float* src = reinterpret_cast<const float*>(smem + C::OFF_STG + (dw * 4 + wq) * 4096);
+                float* dst = p.dq_acc + (row0 + 32) * D + wq * 32 + lane;
+                float vals[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) vals[c] = src[c * 32 + lane];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) red_add_f32(dst + size_t(c) * D, vals[c]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(stg_free);
         }
     }
 
@@ -712,7 +787,7 @@ static int launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
     // one CTA per (key tile, key/value head unit): B * Hkv units token-sharded, P * B * Hkvp head-sharded
     const int units = p.layout == ULYSSES_LAYOUT_TOKEN_SHARDED ? p.B * p.Hkv : p.P * p.B * p.Hkvp;
     dim3 grid(p.n_tiles, units);
-    kern<<<grid, 320, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+    kern<<<grid, bwd_threads<MASK>(), C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
     return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }
 
