@@ -440,17 +440,20 @@ def main():
                                           dv=udv, workspace=uws)
             for _ in range(3):
                 ufwd()
-                ubwd()
+                if w.backward:
+                    ubwd()
             ufwd_ms = cuda_events_time(ufwd, stream, 5)
-            ubwd_ms = cuda_events_time(ubwd, stream, 5)
+            # a forward-only workload times (and credits) the forward alone
+            ubwd_ms = cuda_events_time(ubwd, stream, 5) if w.backward else None
             pairs_fwd = 3 if w.mask == "causal" else 4
             usp = {"P": P_usp, "P_ring": P_ring, "P_u": Pu, "fwd_ms": ufwd_ms, "bwd_ms": ubwd_ms,
                    "fwd_tflops": f_fwd / (ufwd_ms * 1e-3) / 1e12,
                    "bwd_tflops": f_bwd / (ubwd_ms * 1e-3) / 1e12 if w.backward else None,
-                   "fwd_bwd_tflops": (f_fwd + f_bwd) / ((ufwd_ms + ubwd_ms) * 1e-3) / 1e12,
+                   "fwd_bwd_tflops": ((f_fwd + f_bwd) / ((ufwd_ms + ubwd_ms) * 1e-3) / 1e12
+                                      if w.backward else None),
                    # fwd: one attention per block pair + one merge per query block; bwd: one
                    # backward per pair + Delta prep and dQ conversion per query block
-                   "launches_per_step": 2 * pairs_fwd + 3 * P_ring,
+                   "launches_per_step": pairs_fwd + P_ring + ((pairs_fwd + 2 * P_ring) if w.backward else 0),
                    "note": "same tensors and mask, P > H; block-pair attention + merge (fwd), "
                            "block-pair backward + fp32 gradient sums (bwd); not part of the step"}
             del uo, ulse, udq, udk, udv, uws
