@@ -1,6 +1,13 @@
-"""The multi-rank plumbing of bench.py on CPU with the gloo backend (world size 2): the
-barrier, the max-over-ranks timing reduction, and a torchrun launch of the reference arm in
-which only rank 0 works and prints exactly one JSON line."""
+"""Multi-rank paths on CPU with the gloo backend (world size 2).
+
+- bench.py's plumbing: the barrier, the max-over-ranks timing reduction, and a torchrun launch
+  of the reference arm in which only rank 0 works and prints exactly one JSON line.
+- The method's exchanges with one shard per process: the Ulysses sequence-to-head and
+  head-to-sequence all-to-alls around per-head attention, and the USP ring, in which key/value
+  blocks (and, backward, their dK/dV accumulators) travel from rank to rank and the partial
+  results merge by the online-softmax rule. Each rank computes with the fp64 oracle; the
+  assembled O, lse, dQ, dK, dV must equal whole-sequence attention.
+"""
 
 import json
 import os
@@ -56,3 +63,182 @@ def test_reference_arm_under_torchrun_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+# --------------------------------------------------------------------------------------------
+# The method's exchanges across real process boundaries (gloo, CPU). One GPU per run here means
+# the library keeps all P shards in one HBM; these tests run the same decomposition with one
+# shard per process, exchanged by point-to-point messages, and the fp64 oracle as each rank's
+# compute, against whole-sequence attention.
+
+def _init(rank, world, port):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+
+
+def _exchange(send_parts, recv_shapes):
+    """Send send_parts[g] to rank g and receive an array of recv_shapes[s] from each rank s
+    (one's own part is kept): an all-to-all from point-to-point messages."""
+    import numpy as np
+    me, world = dist.get_rank(), dist.get_world_size()
+    reqs = [dist.isend(torch.from_numpy(np.ascontiguousarray(send_parts[g])), dst=g)
+            for g in range(world) if g != me]
+    got = {}
+    for s in range(world):
+        if s == me:
+            got[s] = np.ascontiguousarray(send_parts[me])
+        else:
+            buf = torch.empty(recv_shapes[s], dtype=torch.float64)
+            dist.recv(buf, src=s)
+            got[s] = buf.numpy()
+    for r in reqs:
+        r.wait()
+    return [got[s] for s in range(world)]
+
+
+def _inputs(B, L, H, d, P, seed):
+    import oracle
+    import workloads
+    t = workloads.draw(B, L, H, d, P, seed)
+    return {n: oracle.bf16_to_f64(workloads.to_bf16_bits(x)) for n, x in t.items()}
+
+
+def _ulysses_worker(rank, world, port, out):
+    """Sequence-to-head all-to-all, per-head attention over the full sequence, head-to-sequence
+    all-to-all back (forward and backward), one token shard per rank."""
+    _init(rank, world, port)
+    import numpy as np
+    import oracle
+    B, L, H, d, P = 1, 256, 4, 32, world
+    Lp, Hp = L // P, H // P
+    x = {n: a[rank] for n, a in _inputs(B, L, H, d, P, seed=11).items()}  # this rank's shard [B][Lp][H][d]
+    # seq -> head: head group g gets every rank's tokens of heads [g Hp, (g+1) Hp), in rank order
+    head = {n: np.concatenate(_exchange([a[:, :, g * Hp:(g + 1) * Hp] for g in range(P)], [(B, Lp, Hp, d)] * P),
+                              axis=1) for n, a in x.items()}
+    sc = 1.0 / np.sqrt(d)
+    mask = oracle.Mask("causal")
+    rows = np.arange(L)
+    o = np.zeros((B, L, Hp, d))
+    lse = np.zeros((B, Hp, L))
+    dq, dk, dv = (np.zeros((B, L, Hp, d)) for _ in range(3))
+    for b in range(B):
+        for j in range(Hp):
+            q, k, v, do = (head[n][b, :, j] for n in ("q", "k", "v", "do"))
+            o[b, :, j], lse[b, j] = oracle.head_forward(q, k, v, rows, mask, sc)
+            dq[b, :, j], dk[b, :, j], dv[b, :, j] = oracle.head_backward(q, k, v, do, o[b, :, j], lse[b, j], rows,
+                                                                         mask, sc)
+    # head -> seq: rank s gets its tokens of every head group, heads in group order
+    back = {n: np.concatenate(_exchange([a[:, s * Lp:(s + 1) * Lp] for s in range(P)], [(B, Lp, Hp, d)] * P),
+                              axis=2) for n, a in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv))}
+    back["lse"] = lse
+    out[rank] = back
+    dist.destroy_process_group()
+
+
+def _ring_worker(rank, world, port, out):
+    """The USP ring with P_ring = world and P_u = 1: rank r holds ring block r (all heads). The
+    key/value blocks travel around the ring; each rank attends its query block to every block
+    that reaches it (causal: its own block causally, earlier blocks densely, later ones not at
+    all) and merges the partial results by the online-softmax rule. In the backward pass the
+    key/value blocks travel with their dK, dV accumulators and return to their owners."""
+    _init(rank, world, port)
+    import numpy as np
+    import oracle
+    B, L, H, d, P = 1, 256, 2, 32, world
+    Lb = L // P
+    x = {n: a[rank] for n, a in _inputs(B, L, H, d, P, seed=12).items()}  # ring block [B][Lb][H][d]
+    sc = 1.0 / np.sqrt(d)
+    rows = np.arange(Lb)
+    nxt, prv = (rank + 1) % P, (rank - 1) % P
+
+    def pass_on(arrays):
+        """Send to the next rank, receive the same shapes from the previous one."""
+        reqs = [dist.isend(torch.from_numpy(np.ascontiguousarray(a)), dst=nxt) for a in arrays]
+        got = []
+        for a in arrays:
+            buf = torch.empty(a.shape, dtype=torch.float64)
+            dist.recv(buf, src=prv)
+            got.append(buf.numpy())
+        for r in reqs:
+            r.wait()
+        return got
+
+    def pair_mask(j):
+        return oracle.Mask("causal") if j == rank else (oracle.Mask("none") if j < rank else None)
+
+    # forward: partial (O, lse) per block that reaches this rank, then the merge
+    k, v, j = x["k"], x["v"], rank
+    o_parts, lse_parts = [], []
+    for step in range(P):
+        m = pair_mask(j)
+        if m is not None:
+            o_j = np.zeros((B, H, Lb, d))
+            l_j = np.zeros((B, H, Lb))
+            for b in range(B):
+                for h in range(H):
+                    o_j[b, h], l_j[b, h] = oracle.head_forward(x["q"][b, :, h], k[b, :, h], v[b, :, h], rows, m, sc)
+            o_parts.append(o_j)
+            lse_parts.append(l_j)
+        k, v = pass_on([k, v])
+        j = (j - 1) % P
+    o, lse = oracle.merge_partials(o_parts, lse_parts)  # [B][H][Lb][d], [B][H][Lb]
+    # backward: every block pair's gradient with the merged O and lse
+    k, v, j = x["k"], x["v"], rank
+    dk_acc, dv_acc = np.zeros_like(k), np.zeros_like(v)
+    dq = np.zeros_like(x["q"])
+    for step in range(P):
+        m = pair_mask(j)
+        if m is not None:
+            for b in range(B):
+                for h in range(H):
+                    g_q, g_k, g_v = oracle.head_backward(x["q"][b, :, h], k[b, :, h], v[b, :, h], x["do"][b, :, h],
+                                                         o[b, h], lse[b, h], rows, m, sc)
+                    dq[b, :, h] += g_q
+                    dk_acc[b, :, h] += g_k
+                    dv_acc[b, :, h] += g_v
+        k, v, dk_acc, dv_acc = pass_on([k, v, dk_acc, dv_acc])
+        j = (j - 1) % P
+    assert j == rank  # after a full circle each rank holds its own block and its gradients again
+    out[rank] = {"o": o.transpose(0, 2, 1, 3), "lse": lse, "dq": dq, "dk": dk_acc, "dv": dv_acc}
+    dist.destroy_process_group()
+
+
+def _whole_sequence(B, L, H, d, P, seed):
+    import oracle
+    x = _inputs(B, L, H, d, P, seed)
+    one = {n: a.transpose(1, 0, 2, 3, 4).reshape(1, B, L, H, d) for n, a in x.items()}
+    ref = oracle.attention_full(one["q"], one["k"], one["v"], 1, oracle.Mask("causal"), do_tok=one["do"])
+    return {n: ref[n][0] for n in ("o", "dq", "dk", "dv")}, ref["lse"][0]  # [B][L][H][d], [B][H][L]
+
+
+def _run_ranks(worker, world):
+    port = _free_port()
+    out = mp.get_context("spawn").Manager().dict()
+    mp.spawn(worker, args=(world, port, out), nprocs=world, join=True)
+    return dict(out)
+
+
+@pytest.mark.parametrize("world", [2])
+def test_ulysses_all_to_all_across_ranks_equals_whole_sequence(world):
+    import numpy as np
+    got = _run_ranks(_ulysses_worker, world)
+    ref, ref_lse = _whole_sequence(1, 256, 4, 32, world, seed=11)
+    Lp, Hp = 256 // world, 4 // world
+    for r in range(world):
+        for n in ("o", "dq", "dk", "dv"):
+            assert np.allclose(got[r][n], ref[n][:, r * Lp:(r + 1) * Lp], rtol=1e-10, atol=1e-12), (r, n)
+        # head group r holds the log-sum-exp of its heads over the whole sequence
+        assert np.allclose(got[r]["lse"], ref_lse[:, r * Hp:(r + 1) * Hp], rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("world", [2])
+def test_usp_ring_across_ranks_equals_whole_sequence(world):
+    import numpy as np
+    got = _run_ranks(_ring_worker, world)
+    ref, ref_lse = _whole_sequence(1, 256, 2, 32, world, seed=12)
+    Lb = 256 // world
+    for r in range(world):
+        for n in ("o", "dq", "dk", "dv"):
+            assert np.allclose(got[r][n], ref[n][:, r * Lb:(r + 1) * Lb], rtol=1e-10, atol=1e-12), (r, n)
+        assert np.allclose(got[r]["lse"], ref_lse[:, :, r * Lb:(r + 1) * Lb], rtol=1e-12, atol=1e-12)
