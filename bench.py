@@ -515,8 +515,12 @@ def main():
                             "out_frac": out_flops / (out_ms * 1e-3) / 1e12 / peak_tf,
                             "note": "x [B*L][H*d_h] -> Q, K, V token-sharded; O -> y; not part of the step"},
             "usp": usp,
-            "accounted_alltoall_bytes_per_rank": {"fwd": comm, "leaves_rank": comm * (w.P - 1) // w.P,
-                                                  "note": "4Nh/P in bf16 bytes, accounted, not measured over a link"},
+            # the backward mirrors the forward's exchanges: dO in, dQ out (H heads); dK, dV out
+            # (the key/value heads), the same bytes as Q, O in and K, V
+            "accounted_alltoall_bytes_per_rank": {"fwd": comm, "bwd": comm if w.backward else 0,
+                                                  "leaves_rank": comm * (w.P - 1) // w.P,
+                                                  "note": "4Nh/P in bf16 bytes per pass, accounted, not measured "
+                                                          "over a link; leaves_rank is the forward's (P-1)/P share"},
             "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak_tf,
                          "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": dom_traffic,
                          "peak_source": f"{peak_src} bf16 dense (burst)"},
