@@ -30,10 +30,9 @@ What it computes, and where the pages define it:
   products with the weight matrices (y = x W^T, numpy's fp64 matmul as a library step)
   and keep the token-sharded layout.
 
-Readings where the pages are silent (the plainest one the rest of the pages supports): masked
-positions are
-excluded (-inf), a row with no permitted key has O = 0, LSE = -inf and zero gradients;
-the log-sum-exp is natural-log of the scaled scores, stored [P][B][H/P][L].
+Readings where the pages are silent (the plainest one the rest of the pages supports):
+masked positions are excluded (-inf), a row with no permitted key has O = 0, LSE = -inf and
+zero gradients; the log-sum-exp is natural-log of the scaled scores, stored [P][B][H/P][L].
 """
 
 from __future__ import annotations
