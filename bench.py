@@ -84,6 +84,14 @@ def flops(w: workloads.Workload, fwd_only: bool = False):
     return f_fwd, f_bwd
 
 
+def accounted_alltoall_bytes(w: workloads.Workload) -> int:
+    """bf16 bytes one rank exchanges in the forward pass's two all-to-alls: Q and O with H
+    heads, K and V with H_kv (each head group receives H_kv/P heads, or one copy when
+    P > H_kv). For multi-head attention this is 4Nh/P."""
+    kv_per_group = w.Hkv // w.P if w.Hkv % w.P == 0 else 1
+    return (2 * w.H + 2 * kv_per_group * w.P) * w.B * w.L * w.d * 2 // w.P
+
+
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
 
@@ -489,10 +497,7 @@ def main():
 
     if rank == 0:
         pairs = permitted_pairs(w)
-        # Q and O with H heads, K and V with Hkv (each head group receives Hkv/P heads, or one
-        # copy when P > Hkv): 4Nh/P for multi-head attention
-        kv_per_group = w.Hkv // w.P if w.Hkv % w.P == 0 else 1
-        comm = (2 * w.H + 2 * kv_per_group * w.P) * w.B * w.L * w.d * 2 // w.P
+        comm = accounted_alltoall_bytes(w)
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
