@@ -265,7 +265,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="gpt7b", choices=list(workloads.WORKLOADS))
     ap.add_argument("--L", type=int, default=0, help="override the sequence length (smaller profiling cases)")
-    ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--cpu-rows", type=int, default=3072)
     ap.add_argument("--cpu-heads", type=int, default=4)
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--ref-heads", type=int, default=2)
