@@ -175,6 +175,8 @@ def test_usp_argument_checks(lib):
     assert U.ulysses_usp_workspace_size(s, 1) == 0                               # P_u = 8 does not divide H
     assert U.ulysses_usp_workspace_size(s, 3) == 0                               # 3 does not divide 8
     assert U.ulysses_usp_workspace_size(s, 0) == 0
+    assert U.ulysses_usp_workspace_size(s, 16) == 0                              # P_ring > P
+    assert U.ulysses_usp_workspace_size(s, 65) == 0                              # beyond the ring limit
     assert U.ulysses_usp_workspace_size(U.Shape(1, 512, 4, 96, 8), 2) == 0       # d_h 96
     p = [256 * (i + 1) for i in range(10)]
     ws = 1 << 20

@@ -125,6 +125,10 @@ def test_usp_rejects_bad_splits():
         U.usp_attn_fwd(q, q, q, 8, 1, mask)   # P_u = 8 does not divide H = 4
     with pytest.raises(U.UlyssesError):
         U.usp_attn_fwd(q, q, q, 8, 3, mask)   # P_ring does not divide P
+    with pytest.raises(U.UlyssesError):
+        U.usp_attn_fwd(q, q, q, 8, 16, mask)  # P_ring > P
+    with pytest.raises(U.UlyssesError):
+        U.usp_attn_fwd(q, q, q, 8, 0, mask)   # no ring block
     assert U.ulysses_usp_workspace_size(U.Shape(1, 512, 4, 128, 8, 0), 3) == 0
     assert U.ulysses_usp_workspace_size(U.Shape(1, 512, 4, 128, 8, 0), 2) > 0
 

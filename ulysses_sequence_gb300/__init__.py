@@ -354,11 +354,13 @@ def usp_attn_fwd(q, k, v, P: int, P_ring: int, mask: Mask, scale: float = 0.0, o
     Returns (o, lse[P_ring][P/P_ring][B][H/(P/P_ring)][L/P_ring] fp32)."""
     import torch
     shape = _shape_of(q, P, LAYOUT_TOKEN_SHARDED, k)
-    Pu = P // P_ring
     o = torch.empty_like(q) if o is None else o
     if lse is None:
-        lse = torch.empty((P_ring, Pu, shape.B, shape.H // Pu, shape.L // P_ring), dtype=torch.float32,
-                          device=q.device)
+        # sized for a valid split; the library itself rejects an invalid one
+        valid = P_ring > 0 and P % P_ring == 0 and shape.H % (P // P_ring) == 0
+        Pu = P // P_ring if valid else 1
+        lse = torch.empty((P_ring, Pu, shape.B, shape.H // Pu, shape.L // P_ring) if valid else (1,),
+                          dtype=torch.float32, device=q.device)
     ws = usp_workspace(q, P, P_ring, shape.H_kv) if workspace is None else workspace
     check(ulysses_usp_attn_fwd(shape, P_ring, mask.struct, scale, q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                o.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)), "usp_attn_fwd")
