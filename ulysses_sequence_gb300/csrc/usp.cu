@@ -5,8 +5,8 @@
 // P_u, not P, must divide H). Across blocks, the key/value blocks are streamed past each query
 // block and the per-block attention results are merged with the online-softmax rule:
 //   m = max_j lse_j,  lse = m + ln sum_j exp(lse_j - m),  O = sum_j exp(lse_j - lse) O_j.
-// The block-pair attentions are the library's own forward and backward on tensor slices:
-// causal on the diagonal block pair, every pair below it (or all pairs for a dense mask). The
+// The block-pair attentions are the library's own forward and backward on tensor slices: causal
+// on the diagonal block pair and dense on every pair below it (on all pairs for a dense mask). The
 // backward of a block pair uses the merged O and lse, so its probabilities are those of the
 // whole row; its partial gradients are summed over block pairs in fp32 inside the block-pair
 // backward (its dQ accumulator, and an fp32 store/add mode of its dK, dV epilogue).
