@@ -44,8 +44,8 @@
  *   - Every wait inside a kernel is bounded (about two seconds). A kernel that runs out
  *     of time records the fact in the device error word and returns early; read it with
  *     ulysses_get_device_status(). The word holds (kernel << 24) | (role << 16) | site of the
- *     first wait that gave up: kernel 1 forward, 2 backward, 3 self-test; role 1 loads,
- *     2 MMA issue, 3 softmax, 4 dQ reduction, 5 epilogue, 6 self-test.
+ *     first wait that gave up: kernel 1 forward, 2 backward, 3 self-test, 4 projection
+ *     GEMM; role 1 loads, 2 MMA issue, 3 softmax, 4 dQ reduction, 5 epilogue, 6 self-test.
  */
 #ifndef ULYSSES_H
 #define ULYSSES_H
@@ -139,6 +139,23 @@ int ulysses_kv_seq_to_head(ulysses_shape_t shape, const void *in, void *out, voi
  * Without replication each head has one copy and this is the exact inverse permutation. */
 int ulysses_kv_head_to_seq_sum(ulysses_shape_t shape, const void *in, void *out, void *stream);
 
+/* One rank's side of the two all-to-alls when the P ranks are P processes (paper summary
+ * section 3.4.2 "The All-to-All Communication Primitive"; aifetchly guide, "Explanation of the
+ * Implementation", item 2): the collective itself (an NCCL all-to-all) belongs to the caller,
+ * and these calls lay out its buffers. shape gives the whole problem: B, L (all ranks'
+ * tokens), H (the tensor's own head count: H_kv for keys and values; shape.H_kv is ignored),
+ * d_h and P; it needs H % P == 0 and L % P == 0.
+ *   pack:   in  = this rank's token shard [B][L/P][H][d_h];
+ *           out = [P][B][L/P][H/P][d_h], chunk g (heads [g H/P, (g+1) H/P)) to be sent to rank g:
+ *           out[g][b][t][j][e] = in[b][t][g * H/P + j][e].
+ *   unpack: the inverse: in = the P chunks received, chunk g from the rank holding head
+ *           group g; out = [B][L/P][H][d_h].
+ * With B = 1 the chunks an all-to-all delivers to rank g, concatenated in sender order, are
+ * the head-sharded [L][H/P][d_h] of head group g. 16-bit elements moved unchanged; in and
+ * out must not overlap; 2-byte alignment (16-byte for the vectorised path). */
+int ulysses_a2a_pack(ulysses_shape_t shape, const void *in, void *out, void *stream);
+int ulysses_a2a_unpack(ulysses_shape_t shape, const void *in, void *out, void *stream);
+
 /* Attention forward for every head group (paper summary section 3.4.1 "The challenge at
  * the attention boundary", pinyu.ai page "The layout that saves memory breaks at
  * attention"):  S = scale * Q K^T + mask,  O = softmax(S) V,  lse = ln sum exp(S).
@@ -187,6 +204,9 @@ int ulysses_attn_bwd(ulysses_shape_t shape, const ulysses_mask_t *mask, float so
  *   - Returns ULYSSES_ERR_UNSUPPORTED, launching nothing, when
  *     ulysses_attn_bwd_workspace_size(shape) exceeds ULYSSES_BWD_NOALLOC_SCRATCH_BYTES
  *     (for example B=1, L=8192, H=16, d_h=128 fits; B=1, L=32768, H=32, d_h=128 does not).
+ *     This size check comes first: such a shape returns ULYSSES_ERR_UNSUPPORTED even when
+ *     another argument (mask, layout, d_h, a pointer) is also invalid. Shapes that fit are
+ *     then validated exactly as ulysses_attn_bwd validates them.
  *   - The first call on a device looks up the array's device address with that device
  *     current; make that first call before any stream capture.
  *   - Every call on a device shares the one array, which keeps the contents of the last

@@ -37,6 +37,7 @@ class MaskStruct(ctypes.Structure):
 
 
 EXPORTS = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_kv_seq_to_head", "ulysses_kv_head_to_seq_sum",
+           "ulysses_a2a_pack", "ulysses_a2a_unpack",
            "ulysses_qkv_proj", "ulysses_out_proj", "ulysses_usp_workspace_size", "ulysses_usp_attn_fwd",
            "ulysses_usp_attn_bwd", "ulysses_attn_fwd", "ulysses_attn_bwd_workspace_size",
            "ulysses_attn_bwd", "ulysses_attn_bwd_noalloc", "ulysses_bsmask_build_window_global",
@@ -58,6 +59,8 @@ def load() -> ctypes.CDLL:
     lib.ulysses_seq_to_head.argtypes = [Shape, vp, vp, vp]
     lib.ulysses_head_to_seq.argtypes = [Shape, vp, vp, vp]
     lib.ulysses_kv_seq_to_head.argtypes = [Shape, vp, vp, vp]
+    lib.ulysses_a2a_pack.argtypes = [Shape, vp, vp, vp]
+    lib.ulysses_a2a_unpack.argtypes = [Shape, vp, vp, vp]
     lib.ulysses_qkv_proj.argtypes = [Shape, i, vp, vp, vp, vp, vp, vp]
     lib.ulysses_usp_workspace_size.argtypes = [Shape, i]
     lib.ulysses_usp_workspace_size.restype = sz
@@ -106,6 +109,14 @@ def ulysses_kv_seq_to_head(shape: Shape, inp: int, out: int, stream: int) -> int
 
 def ulysses_kv_head_to_seq_sum(shape: Shape, inp: int, out: int, stream: int) -> int:
     return load().ulysses_kv_head_to_seq_sum(shape, inp, out, stream)
+
+
+def ulysses_a2a_pack(shape: Shape, inp: int, out: int, stream: int) -> int:
+    return load().ulysses_a2a_pack(shape, inp, out, stream)
+
+
+def ulysses_a2a_unpack(shape: Shape, inp: int, out: int, stream: int) -> int:
+    return load().ulysses_a2a_unpack(shape, inp, out, stream)
 
 
 def ulysses_qkv_proj(shape: Shape, hidden: int, x: int, w_qkv: int, q: int, k: int, v: int, stream: int) -> int:
@@ -275,6 +286,28 @@ def head_to_seq(y, P: int, out=None, stream=None):
     if out is None:
         out = torch.empty((P, B, L // P, Hp * P, d), dtype=y.dtype, device=y.device)
     check(ulysses_head_to_seq(head_shape(y, P), y.data_ptr(), out.data_ptr(), _stream(stream)), "head_to_seq")
+    return out
+
+
+def a2a_pack(x, P: int, out=None, stream=None):
+    """One rank's token shard [B][Lp][H][d] -> [P][B][Lp][H/P][d]: chunk g holds head group g,
+    ready for an all-to-all whose rank g owns that group."""
+    import torch
+    B, Lp, H, d = x.shape
+    if out is None:
+        out = torch.empty((P, B, Lp, H // P, d), dtype=x.dtype, device=x.device)
+    check(ulysses_a2a_pack(Shape(B, Lp * P, H, d, P), x.data_ptr(), out.data_ptr(), _stream(stream)), "a2a_pack")
+    return out
+
+
+def a2a_unpack(y, P: int, out=None, stream=None):
+    """Inverse of a2a_pack: [P][B][Lp][H/P][d] (chunk g from head group g) -> [B][Lp][H][d]."""
+    import torch
+    Pn, B, Lp, Hg, d = y.shape
+    if out is None:
+        out = torch.empty((B, Lp, Hg * P, d), dtype=y.dtype, device=y.device)
+    check(ulysses_a2a_unpack(Shape(B, Lp * P, Hg * P, d, P), y.data_ptr(), out.data_ptr(), _stream(stream)),
+          "a2a_unpack")
     return out
 
 

@@ -2,6 +2,8 @@
 // encoding, the per-device error word and the block-sparse tile-list builder.
 #include <cstring>
 #include <mutex>
+#include <set>
+#include <utility>
 #include <vector>
 
 #include "common.cuh"
@@ -55,6 +57,18 @@ int device_sm_count() {
         g_sms[dev] = n;
     }
     return g_sms[dev];
+}
+
+bool set_max_dynamic_smem(const void* fn, int bytes) {
+    const int dev = current_device();
+    if (dev < 0) return false;
+    static std::mutex mu;
+    static std::set<std::pair<const void*, int>> done;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done.count({fn, dev})) return true;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    done.insert({fn, dev});
+    return true;
 }
 
 uint32_t* device_error_word() {
@@ -197,6 +211,36 @@ int ulysses_seq_to_head(ulysses_shape_t shape, const void* in, void* out, void* 
 
 int ulysses_head_to_seq(ulysses_shape_t shape, const void* in, void* out, void* stream) {
     return relayout_common(shape, in, out, stream, false);
+}
+
+// One process's side of the all-to-alls when the P ranks are P processes: its token shard
+// [B][L/P][H][d] split into P contiguous per-destination chunks [P][B][L/P][H/P][d] (pack),
+// and the inverse (unpack). Only B, L, H, d_h and P take part; H is the tensor's own head
+// count (H_kv for keys and values), so H_kv is ignored.
+static int a2a_common(ulysses_shape_t shape, const void* in, void* out, void* stream, bool pack) {
+    if (shape.B < 0 || shape.L < 0 || shape.H <= 0 || shape.d_h <= 0 || shape.P <= 0) return ULYSSES_ERR_INVALID_ARG;
+    if (shape.H % shape.P != 0 || shape.L % shape.P != 0) return ULYSSES_ERR_INVALID_ARG;
+    if (uint64_t(shape.B) * uint64_t(shape.L) * uint64_t(shape.H) * uint64_t(shape.d_h) > (1ull << 40))
+        return ULYSSES_ERR_INVALID_ARG;
+    const uint64_t n = uint64_t(shape.B) * (shape.L / shape.P) * shape.H * shape.d_h;
+    if (n == 0) return ULYSSES_OK;
+    if (!in || !out) return ULYSSES_ERR_INVALID_ARG;
+    if (in == out) return ULYSSES_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 1u) return ULYSSES_ERR_MISALIGNED;
+    // one shard (P = 1) of L / P tokens, split into P head groups
+    ulysses_shape_t one = shape;
+    one.L = shape.L / shape.P;
+    one.P = 1;
+    one.H_kv = 0;
+    return launch_relayout(one, in, out, static_cast<cudaStream_t>(stream), pack, shape.P);
+}
+
+int ulysses_a2a_pack(ulysses_shape_t shape, const void* in, void* out, void* stream) {
+    return a2a_common(shape, in, out, stream, true);
+}
+
+int ulysses_a2a_unpack(ulysses_shape_t shape, const void* in, void* out, void* stream) {
+    return a2a_common(shape, in, out, stream, false);
 }
 
 // Key/value relayouts: without replication they are the plain relayouts of a tensor with

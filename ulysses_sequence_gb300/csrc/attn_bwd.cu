@@ -14,19 +14,20 @@
 //        S^T  = K Q^T     (M=128 keys, N=128 queries, K=d)    -> TMEM columns [0, 128)
 //        dP^T = V dO^T    (M=128, N=128, K=d)                  -> TMEM columns [128, 256)
 //        dV  += P^T dO    (M=128, N=d, K=128)   P^T bf16 in tensor memory over S^T
-//        dK  += dS^T Q    (M=128, N=d, K=128)   dS^T bf16 in tensor memory over dP^T
-//        dQ^T = K^T dS^T  (M=d, N=128, K=128)   dS^T also in shared memory (B operand);
-//                                               written over dP^T once dK has read dS^T,
-//                                               then added into the fp32 accumulator by
-//                                               coalesced 128-byte reductions, half of
-//                                               them from the softmax warps' registers,
-//                                               half staged for two drain warps
+//        dQ^T = K^T dS^T  (M=d, N=128, K=128)   dS^T bf16 in shared memory (B operand),
+//                                               written over dP^T once the softmax warps have
+//                                               read it, then added into the fp32 accumulator
+//                                               by bulk reductions
+//        dK  += dS^T Q    (M=128, N=d, K=128)   the same dS^T buffer as a K-major A operand
 //      The next step's S^T is issued right after dV, so the exponentials of the next P
-//      overlap dK and dQ^T on the tensor cores.
+//      overlap dQ^T and dK on the tensor cores; dQ^T goes before dK, so the drain warps read
+//      it out of tensor memory while dK runs and the next dP^T can follow dK at once.
 //      Warps: 0 TMA producer (K, V once; per step Q into one of two slots, dO into one),
-//      1 MMA issuer, 2-9 softmax / dS / dQ^T read-out, two warps per tensor-memory lane
-//      quadrant, each taking 64 of the step's 128 queries, 10-11 dQ drain. Twelve warps
-//      keep 168 registers per thread (three per sub-partition, as ten already put on two).
+//      1 MMA issuer, 2-9 softmax and dS, two warps per tensor-memory lane quadrant, each
+//      taking 64 of the step's 128 queries, 10-13 dQ drain, one per lane quadrant (and one
+//      per SM sub-partition): each reads its 32 features x 128 queries of dQ^T out of tensor
+//      memory and issues every reduction, so none of them sits in the softmax warps' loop.
+//      Fourteen warps leave 144 registers per thread.
 //   3. bwd_dq_convert: dQ = bf16(scale * accumulator) into the output layout.
 #include <type_traits>
 
@@ -48,7 +49,7 @@ struct BwdParams {
     float scale_log2;
     const float* lse;    // [P][B][Hp][L]
     const float* delta;  // [P][B][Hp][L]
-    float* dq_acc;       // [B*H][n_tiles * 128][D] fp32, rows past L padding
+    float* dq_acc;       // fp32 dQ^T blocks (dq_block), rows past L padding
     void* dk;
     void* dv;
     const int32_t* colptr;  // block-sparse CSC over key tiles
@@ -78,18 +79,16 @@ struct BwdCfg {
     static constexpr uint32_t DST_BYTES = kTile * kQStep * 2;
     static constexpr uint32_t OFF_LSE = OFF_DST + DST_BYTES;    // [2][128] fp32
     static constexpr uint32_t OFF_DELTA = OFF_LSE + 2 * kQStep * 4;  // [2][128] fp32
-    // staging of the softmax warps' dQ^T rows for the drain warps: 32 queries x 32 features
-    // fp32 (4 KB) per softmax warp
+    // each drain warp's private staging of 64 of its dQ^T columns: 32 lanes x 64 fp32 (8 KB)
     static constexpr uint32_t OFF_STG = OFF_DELTA + 2 * kQStep * 4;
-    static constexpr uint32_t STG_BYTES = 8 * 4096;
+    static constexpr uint32_t STG_BYTES = 4 * 8192;
     static constexpr uint32_t OFF_BAR = OFF_STG + STG_BYTES;
     // 1 KB of slack to align the dynamic shared memory base where it fits; without it the
     // kernel checks that the base is 1024-byte aligned (it is, after the 1 KB the system keeps)
     static constexpr uint32_t SLACK = OFF_BAR + 256 + 1024 <= 232448 ? 1024 : 0;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + SLACK;
-    static constexpr int NQ = D / 32 < 4 ? D / 32 : 4;  // lane quadrants that hold dQ^T rows
     static constexpr uint32_t TMEM_COLS = 512;
-    // tensor-memory columns: S^T (then P^T), dP^T (then dS^T, then dQ^T), dV, dK
+    // tensor-memory columns: S^T (then P^T), dP^T (then dQ^T), dV, dK
     static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
     static_assert(T_DK + D <= TMEM_COLS, "tensor memory");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -199,6 +198,18 @@ __device__ __forceinline__ size_t stat_index(const BwdParams& p, int s, int h, i
     return ((size_t(g) * p.B + b) * p.Hp + j) * p.L + s;
 }
 
+// The fp32 dQ accumulator is a sequence of 8 KB blocks, one per (batch x head, query step,
+// query half hq, feature quadrant wq): 32 features x 64 queries of dQ^T, the rows one drain
+// warp reads out of tensor memory. Feature lane l holds its 64 queries as 16 units of four
+// floats, unit u at position u ^ (l & 7), so that the eight lanes of each 128-byte access
+// phase of the warp's 16-byte stores hit different bank groups. A block is added into
+// global memory as it lies in shared memory, by one bulk reduction.
+constexpr uint32_t kDqBlockFloats = 32 * 64;
+template <int D>
+__device__ __forceinline__ size_t dq_block(const BwdParams& p, int bh, int qstep, int hq, int wq) {
+    return ((size_t(bh) * p.n_tiles + qstep) * 2 + hq) * size_t(D / 32) + wq;
+}
+
 template <int MASK>
 __device__ __forceinline__ int bwd_q_count(const BwdParams& p, int kt, int& first) {
     if (MASK == ULYSSES_MASK_CAUSAL) {
@@ -223,15 +234,11 @@ __device__ __forceinline__ int bwd_q_step(const BwdParams& p, int first, int it)
 __device__ __forceinline__ uint32_t a_col(int k) { return uint32_t(8 * k + (k >= 4 ? 64 : 0)); }
 
 // ACC: dK, dV go through the fp32 accumulators (dkv_mode 1-3) instead of straight to bf16
-// Whether the kernel has the two dQ drain warps: the block-sparse variant keeps every reduction
-// in the softmax warps (with the drain its softmax loop spills registers, and measured slower).
-template <int MASK>
-constexpr bool bwd_has_drain() { return MASK != ULYSSES_MASK_BLOCK_SPARSE; }
-template <int MASK>
-constexpr int bwd_threads() { return bwd_has_drain<MASK>() ? 384 : 320; }
+// Warps of the backward kernel: producer, MMA issuer, 8 softmax, 4 dQ drain
+constexpr int kBwdThreads = 14 * 32;
 
 template <int D, int MASK, bool ACC>
-__global__ void __launch_bounds__(bwd_threads<MASK>(), 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const BwdParamsOf<ACC> p) {
@@ -261,12 +268,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint64_t* p_full = bars + 9;      // 8 warps
     uint64_t* ds_full = bars + 10;    // 8 warps
     uint64_t* dq_full = bars + 11;
-    uint64_t* dq_free = bars + 12;    // 8 warps
+    uint64_t* dq_free = bars + 12;    // 4 drain warps
     uint64_t* dkdv_done = bars + 13;
     uint64_t* drain = bars + 14;
-    uint64_t* stg_full = bars + 15;   // softmax warps holding dQ^T rows: rows staged
-    uint64_t* stg_free = bars + 16;   // 2 drain warps: staging slots read out
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = static_cast<int>(warp_id());
@@ -293,11 +298,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(p_full, 8);
         mbar_init(ds_full, 8);
         mbar_init(dq_full, 1);
-        mbar_init(dq_free, 8);
+        mbar_init(dq_free, 4);
         mbar_init(dkdv_done, 1);
         mbar_init(drain, 1);
-        mbar_init(stg_full, 2 * C::NQ);
-        mbar_init(stg_free, 2);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -390,6 +393,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // With d = 64 that block reads the V tile behind K; those lanes of dQ^T are ignored.
             const uint64_t dKt_mn = sdesc_sw128(aK, C::CHUNK, 1024);
             const uint64_t dDSt_mn = sdesc_sw128(aDSt, C::DST_BYTES / 2, 1024);
+            const uint64_t dDSt_k = sdesc_sw128(aDSt, 16, 1024);
             auto issue_s = [&](int j) {  // S^T = K Q^T
                 const uint64_t dQ_k = sdesc_sw128(aQ + (j & 1) * C::T_BYTES, 16, 1024);
 #pragma unroll
@@ -435,20 +439,24 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tc_fence_after();
                     issue_s(it + 1);
                 }
-                // dK += dS^T Q  (dS^T bf16 over dP^T)
+                // dQ^T = K^T dS^T over the dP^T columns (the softmax warps have read dP^T), first,
+                // so that the drain warps read it out while dK runs
                 if (!(ok = mbar_wait(ds_full, it & 1, ab, ROLE_MMA, 6))) break;
                 tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < kQStep / 16; ++k)
-                    umma_ts(tDK, tDP + a_col(k), sdesc_add(dQ_mn, k * 2048), id_kv, (it > 0 || k > 0) ? 1u : 0u);
-                umma_commit(q_empty + (it & 1));
-                // dQ^T = K^T dS^T over the dP^T columns (after dK, which reads dS^T there)
 #pragma unroll
                 for (int k = 0; k < kTile / 16; ++k)
                     umma_ss(tDP, sdesc_add(dKt_mn, k * 2048), sdesc_add(dDSt_mn, k * 2048), id_dq, k > 0 ? 1u : 0u);
                 umma_commit(dq_full);
+                // dK += dS^T Q: dS^T from shared memory as a K-major A operand (its rows are keys
+                // with 64 queries per 128 bytes, the layout the dQ^T MMA reads as MN-major B)
+#pragma unroll
+                for (int k = 0; k < kQStep / 16; ++k) {
+                    const uint32_t o = (k >> 2) * (C::DST_BYTES / 2) + (k & 3) * 32;
+                    umma_ss(tDK, sdesc_add(dDSt_k, o), sdesc_add(dQ_mn, k * 2048), id_kv, (it > 0 || k > 0) ? 1u : 0u);
+                }
+                umma_commit(q_empty + (it & 1));
                 if (more) {
-                    // the next dP^T overwrites dQ^T: wait until the softmax warps have read it
+                    // the next dP^T overwrites dQ^T: wait until the drain warps have read it
                     if (!(ok = mbar_wait(dq_free, it & 1, ab, ROLE_MMA, 7))) break;
                     if (!(ok = mbar_wait(do_full, (it + 1) & 1, ab, ROLE_MMA, 8))) break;
                     tc_fence_after();
@@ -462,7 +470,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
         }
     } else if (warp < 10) {
-        // ------------------------------------------------------------------ softmax, dS, dQ
+        // ------------------------------------------------------------------ softmax, dS
         // thread = one key (tensor-memory lane); half hf takes queries [64 hf, 64 hf + 64)
         const int wq = warp & 3;
         const int hf = (warp - 2) >> 2;
@@ -471,11 +479,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int key = kt * kTile + row;
         // this warp's chunk of the dS^T buffer (64 queries of every key)
         const uint32_t dst_chunk = smem_u32(sDSt) + hf * (C::DST_BYTES / 2);
-        const bool dq_lanes = wq * 32 < D;  // warp-uniform: d = 64 leaves quadrants 2, 3 without dQ rows
         bool ok = true;
         // Per step: dS of this step, then P of the next step (whose S^T the MMA issuer
-        // started right after this step's dV), then this step's dQ^T drain. P is kept in
-        // registers (fp32) from its computation until dS uses it.
+        // started right after this step's dV, so that its exponentials overlap dK and dQ^T).
+        // P is kept in registers (fp32) from its computation until dS uses it.
         float pv[64];
         // P = exp(scale S - lse) of step j over S^T, written back as bf16 P^T (A operand of dV)
         auto softmax_p = [&](int j) -> bool {
@@ -518,9 +525,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (n_it > 0) ok = softmax_p(0);
         for (int it = 0; ok && it < n_it; ++it) {
             const int qs = it & 1;
-            const int ih = it / n_per;
-            const int h = u.h_first + ih;
-            const int qstep = bwd_q_step<MASK>(p, q_first, it - ih * n_per);
             ok = __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, ab, ROLE_SOFTMAX, 3));
             if (!ok) break;
             tc_fence_after();
@@ -546,12 +550,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
-                tmem_st32_u(tmem + C::T_DP + lane_off + 96 * hf, pk);  // A operand of dK
+                // B operand of dQ^T and A operand of dK
 #pragma unroll
-                for (int u = 0; u < 8; ++u)                             // B operand of dQ^T
+                for (int u = 0; u < 8; ++u)
                     st_shared_v4(dst_chunk + sw128_offset(row, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
                                  pk[4 * u + 3]);
-                tmem_wait_st();
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -559,48 +562,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (lane == 0) mbar_arrive(ds_full);
 
             if (it + 1 < n_it && !(ok = softmax_p(it + 1))) break;
-
-            // dQ^T rows of this warp: features [32 wq, 32 wq + 32) (lanes), queries
-            // [64 hf, 64 hf + 64) (columns): one 64-row block of the accumulator
-            ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, ab, ROLE_DQ, 1));
-            if (!ok) break;
-            tc_fence_after();
-            float v[64];
-            tmem_ld32(tmem + C::T_DP + lane_off + 64 * hf, v);
-            tmem_ld32(tmem + C::T_DP + lane_off + 64 * hf + 32, v + 32);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(dq_free);
-            if (dq_lanes && !bwd_has_drain<MASK>()) {
-                // one coalesced 128-byte reduction per query: the warp's 32 lanes are 32
-                // consecutive features of that query's row of the accumulator
-                float* dst = p.dq_acc + (size_t(b * p.H + h) * p.n_tiles * kTile + qstep * kQStep + 64 * hf) * D +
-                             wq * 32 + lane;
-#pragma unroll
-                for (int c = 0; c < 64; ++c) red_add_f32(dst + c * D, v[c]);
-            } else if (dq_lanes) {
-                // The warp's rows of dQ^T: 64 queries x 32 features. Queries [32, 64) are staged
-                // for the drain warps (row = query, lane = feature: each store is one
-                // conflict-free 128-byte row); queries [0, 32) are added here, one coalesced
-                // 128-byte reduction per query. Splitting the reductions between the two groups
-                // of warps takes half of their issue time off this loop, whose length sets
-                // the step (reductions issue faster from more warps, so the drain warps cannot
-                // take them all).
-                if (it > 0) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(stg_free, (it - 1) & 1, ab, ROLE_DQ, 2));
-                    if (!ok) break;
-                }
-                float* r2 = reinterpret_cast<float*>(smem + C::OFF_STG + (hf * 4 + wq) * 4096);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) r2[c * 32 + lane] = v[32 + c];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(stg_full);
-                float* dst = p.dq_acc + (size_t(b * p.H + h) * p.n_tiles * kTile + qstep * kQStep + 64 * hf) * D +
-                             wq * 32 + lane;
-#pragma unroll
-                for (int c = 0; c < 32; ++c) red_add_f32(dst + c * D, v[c]);
-            }
         }
         // ------------------------------------------------------------------ dK, dV epilogue
         if (ok && n_it > 0) ok = __all_sync(0xffffffffu, mbar_wait(dkdv_done, 0, ab, ROLE_EPI, 1));
@@ -647,32 +608,59 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
         }
     } else {
-        // ------------------------------------------------------------------ dQ drain (warps 10, 11)
-        // Drain warp dw adds the rows staged by the softmax warps of query half dw (queries
-        // 64 dw + [32, 64), every feature quadrant) into the fp32 accumulator: each row is
-        // loaded from shared memory first, then added by one coalesced 128-byte reduction.
-        const int dw = warp - 10;
+        // ------------------------------------------------------------------ dQ drain (warps 10-13)
+        // Warp 10 + i reads dQ^T lanes [32 wq, 32 wq + 32) (features, wq = warp % 4, the lane
+        // quadrant this warp may access) for all 128 queries of the step, 64 columns at a time,
+        // and frees the columns for the next dP^T once both halves are in registers or staged.
+        // Each half goes to the warp's 8 KB shared-memory slot in the accumulator's block layout
+        // and is added into global memory by one bulk reduction on the TMA engine, so no warp
+        // issues per-element reductions: those would queue in the same per-sub-partition memory
+        // pipe as the softmax warps' shared-memory traffic and stretch their loop.
+        const int wq = warp & 3;
+        const uint32_t lane_off = uint32_t(wq * 32) << 16;
+        const bool dq_lanes = wq * 32 < D;  // warp-uniform: d = 64 leaves quadrants 2, 3 without dQ rows
+        const uint32_t slot = smem_u32(smem + C::OFF_STG + (warp - 10) * 8192);
+        const uint32_t mine = slot + lane * 256;
+        const uint32_t sw = uint32_t(lane & 7);
         bool ok = true;
+        // one half: wait until the slot's previous bulk reduction has read it, stage, add
+        auto stage_add = [&](const float* v, float* dst) {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+#pragma unroll
+            for (int u4 = 0; u4 < 16; ++u4)
+                st_shared_v4(mine + ((uint32_t(u4) ^ sw) << 4), __float_as_uint(v[4 * u4]), __float_as_uint(v[4 * u4 + 1]),
+                             __float_as_uint(v[4 * u4 + 2]), __float_as_uint(v[4 * u4 + 3]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                bulk_reduce_add_f32(dst, slot, 8192);
+                bulk_commit_group();
+            }
+        };
         for (int it = 0; ok && it < n_it; ++it) {
             const int ih = it / n_per;
             const int h = u.h_first + ih;
             const int qstep = bwd_q_step<MASK>(p, q_first, it - ih * n_per);
-            ok = __all_sync(0xffffffffu, mbar_wait(stg_full, it & 1, ab, ROLE_DQ, 3));
+            ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, ab, ROLE_DQ, 1));
             if (!ok) break;
-            const size_t row0 = size_t(b * p.H + h) * p.n_tiles * kTile + size_t(qstep) * kQStep + 64 * dw;
-#pragma unroll 1
-            for (int wq = 0; wq < C::NQ; ++wq) {
-                const float* src = reinterpret_cast<const float*>(smem + C::OFF_STG + (dw * 4 + wq) * 4096);
-                float* dst = p.dq_acc + (row0 + 32) * D + wq * 32 + lane;
-                float vals[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) vals[c] = src[c * 32 + lane];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) red_add_f32(dst + size_t(c) * D, vals[c]);
-            }
+            tc_fence_after();
+            float v[64];
+            tmem_ld32(tmem + C::T_DP + lane_off, v);
+            tmem_ld32(tmem + C::T_DP + lane_off + 32, v + 32);
+            tmem_wait_ld();
+            float* acc = p.dq_acc + dq_block<D>(p, b * p.H + h, qstep, 0, wq) * kDqBlockFloats;
+            if (dq_lanes) stage_add(v, acc);
+            tmem_ld32(tmem + C::T_DP + lane_off + 64, v);
+            tmem_ld32(tmem + C::T_DP + lane_off + 96, v + 32);
+            tmem_wait_ld();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(stg_free);
+            if (lane == 0) mbar_arrive(dq_free);
+            if (dq_lanes) stage_add(v, acc + size_t(D / 32) * kDqBlockFloats);
         }
+        // the reductions complete before the CTA (and its shared memory) goes away
+        if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -734,29 +722,35 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p, const __nv_b
         acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// dQ = bf16(scale * accumulator), written in the output layout.
+// dQ = bf16(scale * accumulator), written in the output layout. One warp per accumulator
+// block (32 features x 64 queries): lane l reads its feature's 64 values (256 contiguous
+// bytes) and the warp writes, query by query, 32 consecutive features (64 bytes).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdParams p, __nv_bfloat16* dq) {
-    constexpr int LPR = 8;
-    constexpr int VPT = D / (8 * LPR);
-    const size_t rows = size_t(p.B) * p.H * p.L;
-    const int sub = threadIdx.x % LPR;
-    for (size_t rr = (size_t(blockIdx.x) * blockDim.x + threadIdx.x) / LPR; rr < rows;
-         rr += size_t(gridDim.x) * blockDim.x / LPR) {
-        const int s = int(rr % p.L);
-        const size_t bh = rr / p.L;
-        const int h = int(bh % p.H);
-        const int b = int(bh / p.H);
-        const size_t off = row_offset(p, s, h, b, D);
-        const float* acc = p.dq_acc + (bh * p.n_tiles * kTile + s) * size_t(D);
+    constexpr int NQ = D / 32;
+    const size_t blocks = size_t(p.B) * p.H * p.n_tiles * 2 * NQ;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t sw = lane & 7u;
+    for (size_t blk = (size_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32; blk < blocks;
+         blk += size_t(gridDim.x) * blockDim.x / 32) {
+        const int wq = int(blk % NQ);
+        const int hq = int(blk / NQ % 2);
+        const size_t sb = blk / NQ / 2;  // (batch x head, query step)
+        const int qstep = int(sb % p.n_tiles);
+        const int bh = int(sb / p.n_tiles);
+        const int h = bh % p.H, b = bh / p.H;
+        const int s0 = qstep * kQStep + hq * 64;
+        const int e = wq * 32 + int(lane);
+        const float4* src = reinterpret_cast<const float4*>(p.dq_acc + blk * kDqBlockFloats + lane * 64);
+#pragma unroll 4
+        for (int u4 = 0; u4 < 16; ++u4) {
+            const float4 x = src[uint32_t(u4) ^ sw];
+            const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const int e0 = (sub + v * LPR) * 8;
-            const float4 x0 = *reinterpret_cast<const float4*>(acc + e0);
-            const float4 x1 = *reinterpret_cast<const float4*>(acc + e0 + 4);
-            *reinterpret_cast<uint4*>(dq + off + e0) =
-                make_uint4(pack_bf16(x0.x * p.scale, x0.y * p.scale), pack_bf16(x0.z * p.scale, x0.w * p.scale),
-                           pack_bf16(x1.x * p.scale, x1.y * p.scale), pack_bf16(x1.z * p.scale, x1.w * p.scale));
+            for (int c = 0; c < 4; ++c) {
+                const int s = s0 + 4 * u4 + c;
+                if (s < p.L) dq[row_offset(p, s, h, b, D) + e] = __float2bfloat16_rn(xs[c] * p.scale);
+            }
         }
     }
 }
@@ -776,18 +770,11 @@ static int launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
                         const BwdParamsOf<ACC>& p, cudaStream_t stream) {
     using C = BwdCfg<D>;
     auto kern = attn_bwd_kernel<D, MASK, ACC>;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!attr_set[dev & 63]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
-            return ULYSSES_ERR_CUDA;
-        attr_set[dev & 63] = true;
-    }
+    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return ULYSSES_ERR_CUDA;
     // one CTA per (key tile, key/value head unit): B * Hkv units token-sharded, P * B * Hkvp head-sharded
     const int units = p.layout == ULYSSES_LAYOUT_TOKEN_SHARDED ? p.B * p.Hkv : p.P * p.B * p.Hkvp;
     dim3 grid(p.n_tiles, units);
-    kern<<<grid, bwd_threads<MASK>(), C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+    kern<<<grid, kBwdThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
     return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }
 

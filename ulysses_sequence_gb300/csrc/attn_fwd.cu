@@ -469,14 +469,7 @@ static int launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
                         cudaStream_t stream) {
     using C = FwdCfg<D>;
     auto kern = attn_fwd_kernel<D, MASK>;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!attr_set[dev & 63]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
-            return ULYSSES_ERR_CUDA;
-        attr_set[dev & 63] = true;
-    }
+    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return ULYSSES_ERR_CUDA;
     dim3 grid(p.n_pairs, p.B * p.H);
     kern<<<grid, C::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;

@@ -220,15 +220,7 @@ int launch_proj_gemm(int M, int N, int K, const void* a, const void* b, int n_ou
     CUtensorMap ma, mb;
     if (!encode_2d(&ma, a, uint64_t(M), uint64_t(K), C::BM) || !encode_2d(&mb, b, uint64_t(N), uint64_t(K), C::BN))
         return ULYSSES_ERR_CUDA;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!attr_set[dev & 63]) {
-        if (cudaFuncSetAttribute(proj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-            cudaSuccess)
-            return ULYSSES_ERR_CUDA;
-        attr_set[dev & 63] = true;
-    }
+    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(proj_gemm_kernel), C::SMEM_BYTES)) return ULYSSES_ERR_CUDA;
     const int tiles = ((M + C::BM - 1) / C::BM) * ((N + C::BN - 1) / C::BN);
     const int grid = tiles < device_sm_count() ? tiles : device_sm_count();  // persistent: one CTA per SM
     proj_gemm_kernel<<<grid, C::kThreads, C::SMEM_BYTES, stream>>>(ma, mb, p);

@@ -19,6 +19,7 @@ struct RelayoutArgs {
     const void* in;
     void* out;
     uint32_t P, B, Lp, L, H, d;
+    uint32_t G;          // head groups (P for the relayouts; any divisor of H for one rank's packing)
     uint32_t rows;       // token rows P * B * Lp
     uint32_t row_vecs;   // H * d / 8: 16-byte vectors of one token row (P runs)
     uint32_t run_vecs;   // Hp * d / 8: 16-byte vectors of one run
@@ -93,13 +94,13 @@ __global__ void __launch_bounds__(256, 2) relayout_row_kernel(RelayoutArgs a) {
 __global__ void relayout_elem_kernel(RelayoutArgs a, uint64_t total) {
     const uint16_t* in = static_cast<const uint16_t*>(a.in);
     uint16_t* out = static_cast<uint16_t*>(a.out);
-    const uint64_t run_elems = uint64_t(a.H / a.P) * a.d;
+    const uint64_t run_elems = uint64_t(a.H / a.G) * a.d;
     for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += uint64_t(gridDim.x) * blockDim.x) {
         const uint64_t run = i / run_elems;
         const uint64_t e = i - run * run_elems;
-        const uint64_t row = run / a.P;
-        const uint64_t g = run - row * a.P;
+        const uint64_t row = run / a.G;
+        const uint64_t g = run - row * a.G;
         const uint64_t rb = row / a.Lp;
         const uint64_t t = row - rb * a.Lp;
         const uint64_t r = rb / a.B;
@@ -111,15 +112,16 @@ __global__ void relayout_elem_kernel(RelayoutArgs a, uint64_t total) {
     }
 }
 
-int launch_relayout(const ulysses_shape_t& s, const void* in, void* out, cudaStream_t stream, bool to_head) {
+int launch_relayout(const ulysses_shape_t& s, const void* in, void* out, cudaStream_t stream, bool to_head, int G) {
     RelayoutArgs a{};
     a.in = in;
     a.out = out;
-    a.P = s.P; a.B = s.B; a.L = s.L; a.Lp = s.L / s.P; a.H = s.H; a.d = s.d_h;
+    if (G <= 0) G = s.P;
+    a.P = s.P; a.B = s.B; a.L = s.L; a.Lp = s.L / s.P; a.H = s.H; a.d = s.d_h; a.G = uint32_t(G);
     a.to_head = to_head ? 1 : 0;
     const uint64_t rows = uint64_t(s.P) * s.B * a.Lp;
     const uint64_t row_elems = uint64_t(s.H) * s.d_h;
-    const uint64_t run_elems = row_elems / s.P;
+    const uint64_t run_elems = row_elems / uint64_t(G);
     const uint64_t total = rows * row_elems;
     if (total == 0) return ULYSSES_OK;
     const int sms = device_sm_count();

@@ -13,6 +13,9 @@ constexpr int kTile = 128;      // query / key tile edge of the attention kernel
 constexpr int kBwdQTile = 64;   // query rows per step of the backward kernel
 
 int device_sm_count();
+// Raises kernel fn's dynamic shared-memory limit to `bytes` on the current device, once per
+// (kernel, device): thread-safe, and a failed attempt is retried by the next call.
+bool set_max_dynamic_smem(const void* fn, int bytes);
 uint32_t* device_error_word();  // device address of this device's error word (nullptr on failure)
 
 // Key/value head arrangement of a shape (grouped-query attention when Hkv < H).
@@ -53,7 +56,10 @@ struct MaskArgs {
     const int32_t* k_qrows;
 };
 
-int launch_relayout(const ulysses_shape_t& s, const void* in, void* out, cudaStream_t stream, bool to_head);
+// The token <-> head relayouts over P shards and G head groups (G <= 0: G = P). With P = 1 and
+// G > 1 it packs one rank's token shard into G per-destination chunks (or unpacks them).
+int launch_relayout(const ulysses_shape_t& s, const void* in, void* out, cudaStream_t stream, bool to_head,
+                    int G = 0);
 // Key/value relayouts with replication (P > Hkv): seq->head copies, head->seq sums the copies.
 int launch_kv_replicated(const ulysses_shape_t& s, const void* in, void* out, cudaStream_t stream, bool to_head);
 
