@@ -172,27 +172,46 @@ def test_gpt1p2b_forward_every_row():
     check_all({"o": f64(o), "lse": lse.cpu().double().numpy()}, ref, backward=False)
 
 
-# Long: all 4096 rows on 8 of its 32 heads (each head is its own group at P=32), to keep
-# the fp64 oracle within about a minute; the grouped-query layer checks the 12 query heads
-# of its key/value heads 0, 3 and 7; the other two check every head.
-SAMPLED = [("gpt7b", None), ("long", (0, 4, 9, 13, 18, 22, 27, 31)), ("block_sparse", None),
-           ("gpt7b_gqa", (0, 1, 2, 3, 12, 13, 14, 15, 28, 29, 30, 31))]
+# gpt7b and block_sparse check all 4096 rows on every head. Long and the grouped-query layer
+# check every head too, each on its own quarter of the rows (query head h takes the sampled
+# rows whose index is h mod 4, plus the first and last row of the sequence): at P=32 each head
+# of Long is its own head group, so all 32 groups' fused relayouts are compared, and the fp64
+# oracle does the work of 8 whole heads; every key/value head of the grouped layer sees all
+# 4096 rows through its 4 query heads.
+SAMPLED = [("gpt7b", False), ("long", True), ("block_sparse", False), ("gpt7b_gqa", True)]
 
 
-@pytest.mark.parametrize("name,heads", SAMPLED, ids=[s[0] for s in SAMPLED])
-def test_large_workload_sampled_rows(name, heads):
+def _head_rows(rows: np.ndarray, L: int, H: int, split: bool):
+    """[(heads, rows)] groups for the oracle: every head with every row, or heads h = r mod 4
+    with the rows of index r mod 4 (plus the sequence's first and last rows)."""
+    if not split:
+        return [(tuple(range(H)), rows)]
+    edge = rows[(rows[:, 0] == 0) & ((rows[:, 1] == 0) | (rows[:, 1] == L - 1))]
+    out = []
+    for r in range(4):
+        sub = np.unique(np.concatenate([edge, rows[r::4]]), axis=0)
+        out.append((tuple(range(r, H, 4)), sub))
+    return out
+
+
+@pytest.mark.parametrize("name,split", SAMPLED, ids=[s[0] for s in SAMPLED])
+def test_large_workload_sampled_rows(name, split):
     """4096 seeded query rows: O, lse and dQ of those rows from a pass with the full dO
-    (run A), and dK, dV over every key from a pass whose dO is zero outside those rows
-    (run B), which then hold exactly the sampled rows' gradient contributions. With grouped
-    key/value heads, dK and dV are compared with the sum of the contributions of the query
-    heads of each key/value head whose whole group is checked."""
+    (run A), and dK, dV over every key from a pass whose dO is zero outside the checked
+    (row, head) pairs (run B), which then hold exactly their gradient contributions. With
+    grouped key/value heads, dK and dV are compared with the sum of the contributions of the
+    query heads of each key/value head."""
     w = workloads.WORKLOADS[name]
     t = workloads.draw_workload(w)
     P, B, L, H, d = w.P, w.B, w.L, w.H, w.d
     rows = workloads.sample_rows(B, L, env_rows(w.sampled_rows), seed=w.seed)
-    keep = torch.zeros((B, L), dtype=torch.bool)
-    keep[torch.from_numpy(rows[:, 0]), torch.from_numpy(rows[:, 1])] = True
-    keep_tok = keep.reshape(B, P, L // P).permute(1, 0, 2)[..., None, None]
+    groups = _head_rows(rows, L, H, split)
+    keep = torch.zeros((B, L, H), dtype=torch.bool)
+    for hs, rr in groups:
+        sel = keep[torch.from_numpy(rr[:, 0]), torch.from_numpy(rr[:, 1])]
+        sel[:, list(hs)] = True
+        keep[torch.from_numpy(rr[:, 0]), torch.from_numpy(rr[:, 1])] = sel
+    keep_tok = keep.reshape(B, P, L // P, H).permute(1, 0, 2, 3)[..., None]
     dev = {n: x.cuda() for n, x in t.items()}
     mask = gpu_mask(w.mask, L, w=w) if w.mask == "block_sparse" else gpu_mask(w.mask, L)
     o, lse = U.attn_fwd(dev["q"], dev["k"], dev["v"], P, mask)
@@ -208,7 +227,7 @@ def test_large_workload_sampled_rows(name, heads):
 
     O, dQA, dQB, dKB, dVB = (logical_t(x) for x in (o, dqA, dqB, dkB, dvB))
     LSE = lse.cpu().permute(1, 0, 2, 3).reshape(B, H, L)
-    # rows outside the sample get no dQ in run B
+    # (row, head) pairs outside the checked set get no dQ in run B
     assert torch.count_nonzero(dQB.float()[~keep]) == 0
     del dev, o, dqA, dqB, dkB, dvB, do_b
     torch.cuda.empty_cache()
@@ -219,23 +238,27 @@ def test_large_workload_sampled_rows(name, heads):
     lse_err = 0.0
     bits = {n: workloads.to_bf16_bits(x) for n, x in t.items()}
     workers = min(8, os.cpu_count() or 1)
-    for res in oracle.attention_sampled(bits["q"], bits["k"], bits["v"], bits["do"], P, oracle.mask_for(w), rows,
-                                        heads=heads, workers=workers):
-        b, h, r = res["b"], res["h"], torch.from_numpy(res["rows"])
-        stats["o"].add(O[b, r, h].double().numpy(), res["o"])
-        stats["dq"].add(dQA[b, r, h].double().numpy(), res["dq"])
-        acc = kv_ref.setdefault((b, res["kvh"]), [0.0, 0.0, 0])
-        acc[0] = acc[0] + res["dk"]
-        acc[1] = acc[1] + res["dv"]
-        acc[2] += 1
-        lse_err = max(lse_err, float(np.abs(LSE[b, h, r].double().numpy() - res["lse"]).max()))
+    seen = set()
+    for hs, rr in groups:
+        for res in oracle.attention_sampled(bits["q"], bits["k"], bits["v"], bits["do"], P, oracle.mask_for(w), rr,
+                                            heads=hs, workers=workers):
+            b, h, r = res["b"], res["h"], torch.from_numpy(res["rows"])
+            seen.add(h)
+            stats["o"].add(O[b, r, h].double().numpy(), res["o"])
+            stats["dq"].add(dQA[b, r, h].double().numpy(), res["dq"])
+            acc = kv_ref.setdefault((b, res["kvh"]), [0.0, 0.0, 0])
+            acc[0] = acc[0] + res["dk"]
+            acc[1] = acc[1] + res["dv"]
+            acc[2] += 1
+            lse_err = max(lse_err, float(np.abs(LSE[b, h, r].double().numpy() - res["lse"]).max()))
+    assert seen == set(range(H))
     excess = 0.0  # grouped heads: largest error beyond the bf16 rounding of the summed gradient
     for (b, kvh), (rdk, rdv, n) in kv_ref.items():
-        if n == G:
-            for name, got, ref in (("dk", dKB[b, :, kvh], rdk), ("dv", dVB[b, :, kvh], rdv)):
-                g64 = got.double().numpy()
-                stats[name].add(g64, ref)
-                excess = max(excess, float((np.abs(g64 - ref) - 2.0 ** -8 * np.abs(ref)).max()))
+        assert n == G
+        for name, got, ref in (("dk", dKB[b, :, kvh], rdk), ("dv", dVB[b, :, kvh], rdv)):
+            g64 = got.double().numpy()
+            stats[name].add(g64, ref)
+            excess = max(excess, float((np.abs(g64 - ref) - 2.0 ** -8 * np.abs(ref)).max()))
     for n, s in stats.items():
         # with grouped key/value heads dK, dV sum G query heads' gradients and grow with G: their
         # bound adds the one bf16 rounding of the result (see test_gqa_gpu.py)

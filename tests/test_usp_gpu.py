@@ -62,19 +62,22 @@ def _run(B, L, H, Hkv, d, P, P_ring, kind, seed):
     return got, ref
 
 
-def _check(got, ref):
-    s = ErrStats("o")
-    s.add(got["o"], ref["o"])
-    s.check()
-    # dQ, dK, dV are summed over block pairs in fp32 and rounded once, but grouped dK, dV also sum
-    # the G query heads of a key/value head and so grow with G: as for grouped heads, the bound
-    # adds half a bf16 unit of the result (2^-9 relative), doubled, to the absolute tolerance
-    for n in ("dq", "dk", "dv"):
+def _check(got, ref, grouped):
+    """O and dQ always meet the acceptance bound (max-abs 2e-2, rel-L2 5e-3): every block pair's
+    part is summed in fp32 and rounded once, exactly as in plain Ulysses. So do dK and dV when
+    every query head has its own key/value head. Only grouped dK, dV (H_kv < H) take the grouped
+    reading's elementwise bound 2e-2 + 2^-8 |ref|: they sum the gradients of G query heads, so
+    they grow with G, and the single bf16 rounding of that larger result adds half a unit
+    (2^-9 relative), doubled in the bound; their rel-L2 bound stays 5e-3."""
+    for n in ("o", "dq", "dk", "dv"):
         s = ErrStats(n)
         s.add(got[n], ref[n])
-        s.check(max_abs=None)
-        err = np.abs(got[n] - ref[n])
-        assert np.all(err <= 2e-2 + 2.0 ** -8 * np.abs(ref[n])), (n, float(err.max()))
+        if grouped and n in ("dk", "dv"):
+            s.check(max_abs=None)
+            err = np.abs(got[n] - ref[n])
+            assert np.all(err <= 2e-2 + 2.0 ** -8 * np.abs(ref[n])), (n, float(err.max()))
+        else:
+            s.check()
     fin = np.isfinite(ref["lse"])
     assert np.array_equal(np.isneginf(got["lse"]), np.isneginf(ref["lse"]))
     assert np.abs(got["lse"][fin] - ref["lse"][fin]).max() <= LSE_MAX_ABS
@@ -96,7 +99,7 @@ CASES = [
 @pytest.mark.parametrize("name,B,L,H,Hkv,d,P,P_ring,kind", CASES, ids=[c[0] for c in CASES])
 def test_usp_every_row(name, B, L, H, Hkv, d, P, P_ring, kind):
     got, ref = _run(B, L, H, Hkv, d, P, P_ring, kind, seed=sum(map(ord, name)))
-    _check(got, ref)
+    _check(got, ref, grouped=Hkv < H)
 
 
 def test_usp_ring1_is_plain_ulysses():
