@@ -40,8 +40,8 @@ import workloads  # noqa: E402
 METRIC = "Ulysses attn fwd+bwd TFLOP/s & % BF16 peak; relayout HBM GB/s"
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the attention kernels
-# on the full-size GPT-7B-like layer, from single-pass ncu captures summarised in
-# profiles/attn_kernels_gpt7b.md. A figure is reported only while the kernel sources still
+# on the full-size GPT-7B-like layer, from single-pass ncu captures of that workload (the
+# summaries sit under profiles/). A figure is reported only while the kernel sources still
 # hash to the value recorded with it; after any change it reads as null until re-captured.
 NCU_TRAFFIC = {
     "attn_bwd_kernel": {"bytes": 2645448192, "workload": "gpt7b", "sha": "881321f88a752b82",
@@ -156,13 +156,20 @@ def measured_peaks():
     return 1900.0, 6800.0, "fallback"
 
 
-def dist_setup():
+def dist_setup(force: bool = False):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
+    if world > 1 or force:
         import torch.distributed as dist
         backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if world == 1:
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            os.environ.setdefault("MASTER_PORT", "29511")
+            os.environ.setdefault("RANK", "0")
+            os.environ.setdefault("WORLD_SIZE", "1")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
         dist.init_process_group(backend)
     return world, rank, local
 
@@ -244,6 +251,121 @@ def run_reference(args, w, world, rank):
     return 0
 
 
+# ----------------------------------------------------------------------------- GPU arm, N > 1
+
+def run_distributed(args, w, world, rank, local):
+    """The layer over `world` GPUs as real Ulysses ranks: each process owns L/world tokens of
+    every head on its own GPU, the two all-to-alls per pass run through NCCL
+    (ulysses_sequence_gb300.distributed), and each rank attends over the whole sequence for
+    its H/world heads. The total work is the one layer's, so this is strong scaling."""
+    import ulysses_sequence_gb300 as U
+    from ulysses_sequence_gb300.distributed import UlyssesAttention
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    if w.H % world or w.Hkv % world or w.L % world:
+        raise SystemExit(f"{w.name}: H={w.H}, H_kv={w.Hkv} and L={w.L} must split over {world} ranks")
+    f_fwd, f_bwd = flops(w)
+    total_flops = f_fwd + f_bwd
+    # the same logical tensors on every rank; this rank keeps its token shard [B][L/world][H][d]
+    t = workloads.draw(w.B, w.L, w.H, w.d, world, w.seed, q_scale=w.q_scale, H_kv=w.H_kv)
+    host = {n: x[rank].contiguous().pin_memory() for n, x in t.items()}
+    del t
+    x = {n: v.to(dev) for n, v in host.items()}
+    mask = U.Mask.causal() if w.mask == "causal" else (
+        U.Mask.none() if w.mask == "none" else
+        U.Mask.window_global(w.L, w.tile, w.window_before, w.window_after, w.global_stride, device=dev))
+    ua = UlyssesAttention(mask=mask)
+
+    def step(inp):
+        o, ctx = ua.forward(inp["q"], inp["k"], inp["v"])
+        if not w.backward:
+            return (o,), ctx
+        return (o,) + ua.backward(ctx, inp["do"]), ctx
+
+    for _ in range(args.warmup):
+        step(x)
+    torch.cuda.synchronize()
+    st, word = U.device_status()
+    U.check(st, f"device status after warm-up ({word:#x})")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(x)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    ms_per_step = elapsed_ms / args.steps
+    value = total_flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # the local attention alone (this rank's head group, inputs already exchanged)
+    outs, ctx = step(x)
+    qh, kh, vh, oh, lse = ctx
+    doh = ua.to_heads(x["do"]) if w.backward else None
+    fwd_ms = cuda_events_time(lambda: ua.ops.attn_fwd(qh, kh, vh), stream, 3)
+    bwd_ms = cuda_events_time(lambda: ua.ops.attn_bwd(qh, kh, vh, oh, lse, doh), stream, 3) if w.backward else 0.0
+    fwd_ms, bwd_ms = max_over_ranks(fwd_ms, world), max_over_ranks(bwd_ms, world)
+
+    # end to end: this rank's shards from pinned host memory, results back, every step
+    out_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    dev_in = {n: torch.empty_like(v) for n, v in x.items()}
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        for n in dev_in:
+            dev_in[n].copy_(host[n], non_blocking=True)
+        res, _ = step(dev_in)
+        for h, r in zip(out_host, res):
+            h.copy_(r, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    st, word = U.device_status()
+    U.check(st, f"device status after timed steps ({word:#x})")
+    peak_tf, _, peak_src = measured_peaks()
+    dom_ms, dom_flops, dom_name = (bwd_ms, f_bwd / world, "attn_bwd (local head group)") if w.backward else (
+        fwd_ms, f_fwd / world, "attn_fwd (local head group)")
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    if rank == 0:
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = sum(h.numel() * h.element_size() for h in out_host)
+        comm = w.B * w.L * (2 * w.H + 2 * w.Hkv) * w.d * 2 // world  # Q, K, V in and O out, bf16, per rank
+        kernels = (4 * w.B + 1) + ((4 * w.B + 3) if w.backward else 0)
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "strong",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "H_kv": w.Hkv, "d_h": w.d, "P": world,
+                       "mask": w.mask, "passes": "fwd+bwd" if w.backward else "fwd",
+                       "l2": "inputs larger than L2 (the layer's 4 tensors)",
+                       "parallelism": f"ulysses sp{world}: one token shard per GPU, NCCL all-to-all"},
+            "frac_of_peak": value / world / peak_tf,
+            "local_fwd_ms": fwd_ms, "local_bwd_ms": bwd_ms,
+            "alltoall_bytes_per_rank_per_pass": comm,
+            "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak_tf,
+                         "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": None,
+                         "peak_source": f"{peak_src} bf16 dense (burst)"},
+            "cpu_baseline": None,
+            "e2e": {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "note": "per rank: its token shards in from pinned host memory, its results out"},
+            "gpu_launches": args.steps * kernels,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    import torch.distributed as dist
+    dist.destroy_process_group()
+    return 0
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def cuda_events_time(fn, stream, iters):
@@ -270,15 +392,19 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--ref-heads", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dist", action="store_true",
+                    help="run the multi-process Ulysses path (NCCL all-to-alls) even on one GPU")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = workloads.WORKLOADS[args.workload]
     if args.L:
         import dataclasses
         w = dataclasses.replace(w, name=f"{w.name}@L{args.L}", L=args.L)
-    world, rank, local = dist_setup()
+    world, rank, local = dist_setup(force=args.dist and args.impl != "reference")
     if args.impl == "reference":
         return run_reference(args, w, world, rank)
+    if world > 1 or args.dist:
+        return run_distributed(args, w, world, rank, local)
 
     import ulysses_sequence_gb300 as U
     torch.cuda.set_device(local)
@@ -490,10 +616,26 @@ def main():
             dt = time.perf_counter() - t0
             cpu = {"value": fc / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                    "sample": f"{len(rows)} sampled query rows x {len(heads_s)} heads of {w.name}, fwd+bwd "
-                             f"({fc / 1e9:.1f} GFLOP in {dt:.1f} s)"}
+                             f"({fc / 1e9:.1f} GFLOP in {dt:.1f} s)",
+                   # the sample's time scaled to the whole workload by algorithmic flops (the
+                   # sampled rows' permitted pairs against all of them): an extrapolation, not a run
+                   "full_workload_s_extrapolated": dt * total_flops / fc,
+                   "extrapolation": "t_sample x flops(workload) / flops(sample); not measured"}
         except Exception as exc:  # the baseline must not hide the GPU line
             cpu = {"value": None, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                    "sample": f"failed: {exc}"}
+
+    # The chip's nominal dense bf16 rate: SMs x SM clock x 8192 flops per clock per SM (one
+    # M=128, N=256, K=16 tcgen05 MMA, 2*128*256*16 flops, every 128 cycles: twice the previous
+    # generation's 4096), at the median SM clock sampled in the timed region
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    nom_mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz")
+    nominal = None
+    if nom_mhz:
+        nom_tf = sms * nom_mhz * 1e6 * 8192 / 1e12
+        nominal = {"tflops": nom_tf, "sms": sms, "sm_mhz": nom_mhz, "flops_per_clk_per_sm": 8192,
+                   "frac": value / world / nom_tf, "roofline_frac": achieved / nom_tf,
+                   "note": "SM count x sampled SM clock x 8192 bf16 flops/clk/SM; beside the measured peak"}
 
     if rank == 0:
         pairs = permitted_pairs(w)
@@ -529,6 +671,7 @@ def main():
             "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak_tf,
                          "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": dom_traffic,
                          "peak_source": f"{peak_src} bf16 dense (burst)"},
+            "nominal_peak": nominal,
             "cpu_baseline": cpu,
             "e2e": {"value": total_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,

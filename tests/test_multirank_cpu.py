@@ -2,8 +2,10 @@
 
 - bench.py's plumbing: the barrier, the max-over-ranks timing reduction, and a torchrun launch
   of the reference arm in which only rank 0 works and prints exactly one JSON line.
-- The method's exchanges with one shard per process: the Ulysses sequence-to-head and
-  head-to-sequence all-to-alls around per-head attention, and the USP ring, in which key/value
+- The method's exchanges with one shard per process: the package's Ulysses layer
+  (ulysses_sequence_gb300.distributed: pack, all_to_all_single, per-head-group attention,
+  all_to_all_single, unpack) driven over gloo with the oracle as each rank's local attention,
+  and the USP ring, in which key/value
   blocks (and, backward, their dK/dV accumulators) travel from rank to rank and the partial
   results merge by the online-softmax rule. Each rank computes with the fp64 oracle; the
   assembled O, lse, dQ, dK, dV must equal whole-sequence attention.
@@ -104,35 +106,80 @@ def _inputs(B, L, H, d, P, seed):
     return {n: oracle.bf16_to_f64(workloads.to_bf16_bits(x)) for n, x in t.items()}
 
 
-def _ulysses_worker(rank, world, port, out):
-    """Sequence-to-head all-to-all, per-head attention over the full sequence, head-to-sequence
-    all-to-all back (forward and backward), one token shard per rank."""
+class _OracleOps:
+    """Local steps on the CPU for the package's exchange code (UlyssesAttention): packing and
+    unpacking written here with torch views, attention by the fp64 oracle per (batch, head)."""
+
+    def __init__(self):
+        import oracle
+        self.oracle = oracle
+        self.mask = oracle.Mask("causal")
+
+    def empty(self, shape, like):
+        return torch.empty(shape, dtype=torch.float64)
+
+    def pack(self, x, P):
+        B, Lp, H, d = x.shape
+        return x.reshape(B, Lp, P, H // P, d).permute(2, 0, 1, 3, 4).contiguous()
+
+    def unpack(self, y, P, out):
+        Pn, B, Lp, Hg, d = y.shape
+        out.copy_(y.permute(1, 2, 0, 3, 4).reshape(B, Lp, P * Hg, d))
+        return out
+
+    def _kv(self, j, Hg, Hkvg):
+        return j // (Hg // Hkvg)
+
+    def attn_fwd(self, q, k, v):
+        import numpy as np
+        B, L, Hg, d = q.shape
+        rows = np.arange(L)
+        sc = 1.0 / np.sqrt(d)
+        o = np.zeros((B, L, Hg, d))
+        lse = np.zeros((1, B, Hg, L))
+        for b in range(B):
+            for j in range(Hg):
+                kj = self._kv(j, Hg, k.shape[2])
+                o[b, :, j], lse[0, b, j] = self.oracle.head_forward(q[b, :, j].numpy(), k[b, :, kj].numpy(),
+                                                                    v[b, :, kj].numpy(), rows, self.mask, sc)
+        return torch.from_numpy(o), torch.from_numpy(lse)
+
+    def attn_bwd(self, q, k, v, o, lse, do):
+        import numpy as np
+        B, L, Hg, d = q.shape
+        rows = np.arange(L)
+        sc = 1.0 / np.sqrt(d)
+        dq = np.zeros((B, L, Hg, d))
+        dk, dv = np.zeros(tuple(k.shape)), np.zeros(tuple(v.shape))
+        for b in range(B):
+            for j in range(Hg):
+                kj = self._kv(j, Hg, k.shape[2])
+                g = self.oracle.head_backward(q[b, :, j].numpy(), k[b, :, kj].numpy(), v[b, :, kj].numpy(),
+                                              do[b, :, j].numpy(), o[b, :, j].numpy(), lse[0, b, j].numpy(), rows,
+                                              self.mask, sc)
+                dq[b, :, j] = g[0]
+                dk[b, :, kj] += g[1]
+                dv[b, :, kj] += g[2]
+        return torch.from_numpy(dq), torch.from_numpy(dk), torch.from_numpy(dv)
+
+
+ULY_CASES = {"mha": (2, 256, 4, 4, 32), "gqa": (1, 256, 8, 4, 32)}  # B, L, H, H_kv, d
+
+
+def _ulysses_worker(rank, world, port, out, case):
+    """The package's two all-to-alls (UlyssesAttention over gloo), one token shard per rank, the
+    fp64 oracle as each rank's local attention, forward and backward."""
     _init(rank, world, port)
-    import numpy as np
+    import workloads
+    from ulysses_sequence_gb300.distributed import UlyssesAttention
     import oracle
-    B, L, H, d, P = 1, 256, 4, 32, world
-    Lp, Hp = L // P, H // P
-    x = {n: a[rank] for n, a in _inputs(B, L, H, d, P, seed=11).items()}  # this rank's shard [B][Lp][H][d]
-    # seq -> head: head group g gets every rank's tokens of heads [g Hp, (g+1) Hp), in rank order
-    head = {n: np.concatenate(_exchange([a[:, :, g * Hp:(g + 1) * Hp] for g in range(P)], [(B, Lp, Hp, d)] * P),
-                              axis=1) for n, a in x.items()}
-    sc = 1.0 / np.sqrt(d)
-    mask = oracle.Mask("causal")
-    rows = np.arange(L)
-    o = np.zeros((B, L, Hp, d))
-    lse = np.zeros((B, Hp, L))
-    dq, dk, dv = (np.zeros((B, L, Hp, d)) for _ in range(3))
-    for b in range(B):
-        for j in range(Hp):
-            q, k, v, do = (head[n][b, :, j] for n in ("q", "k", "v", "do"))
-            o[b, :, j], lse[b, j] = oracle.head_forward(q, k, v, rows, mask, sc)
-            dq[b, :, j], dk[b, :, j], dv[b, :, j] = oracle.head_backward(q, k, v, do, o[b, :, j], lse[b, j], rows,
-                                                                         mask, sc)
-    # head -> seq: rank s gets its tokens of every head group, heads in group order
-    back = {n: np.concatenate(_exchange([a[:, s * Lp:(s + 1) * Lp] for s in range(P)], [(B, Lp, Hp, d)] * P),
-                              axis=2) for n, a in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv))}
-    back["lse"] = lse
-    out[rank] = back
+    B, L, H, Hkv, d = ULY_CASES[case]
+    t = workloads.draw(B, L, H, d, world, seed=11, H_kv=Hkv)
+    x = {n: torch.from_numpy(oracle.bf16_to_f64(workloads.to_bf16_bits(a))[rank]) for n, a in t.items()}
+    ua = UlyssesAttention(ops=_OracleOps())
+    o, ctx = ua.forward(x["q"], x["k"], x["v"])
+    dq, dk, dv = ua.backward(ctx, x["do"])
+    out[rank] = {"o": o.numpy(), "dq": dq.numpy(), "dk": dk.numpy(), "dv": dv.numpy(), "lse": ctx[4][0].numpy()}
     dist.destroy_process_group()
 
 
@@ -219,17 +266,27 @@ def _run_ranks(worker, world):
     return dict(out)
 
 
-@pytest.mark.parametrize("world", [2])
-def test_ulysses_all_to_all_across_ranks_equals_whole_sequence(world):
+@pytest.mark.parametrize("world,case", [(2, "mha"), (4, "gqa")])
+def test_ulysses_all_to_all_across_ranks_equals_whole_sequence(world, case):
+    """ulysses_sequence_gb300.distributed on gloo: every rank's O, dQ, dK, dV (its tokens) and
+    lse (its head group) equal attention over the whole sequence."""
     import numpy as np
-    got = _run_ranks(_ulysses_worker, world)
-    ref, ref_lse = _whole_sequence(1, 256, 4, 32, world, seed=11)
-    Lp, Hp = 256 // world, 4 // world
+    import oracle
+    import workloads
+    port = _free_port()
+    res = mp.get_context("spawn").Manager().dict()
+    mp.spawn(_ulysses_worker, args=(world, port, res, case), nprocs=world, join=True)
+    got = dict(res)
+    B, L, H, Hkv, d = ULY_CASES[case]
+    t = workloads.draw(B, L, H, d, world, seed=11, H_kv=Hkv)
+    x = {n: oracle.bf16_to_f64(workloads.to_bf16_bits(a)) for n, a in t.items()}
+    one = {n: a.transpose(1, 0, 2, 3, 4).reshape(1, B, L, a.shape[3], d) for n, a in x.items()}
+    ref = oracle.attention_full(one["q"], one["k"], one["v"], 1, oracle.Mask("causal"), do_tok=one["do"])
+    Lp, Hp = L // world, H // world
     for r in range(world):
         for n in ("o", "dq", "dk", "dv"):
-            assert np.allclose(got[r][n], ref[n][:, r * Lp:(r + 1) * Lp], rtol=1e-10, atol=1e-12), (r, n)
-        # head group r holds the log-sum-exp of its heads over the whole sequence
-        assert np.allclose(got[r]["lse"], ref_lse[:, r * Hp:(r + 1) * Hp], rtol=1e-12, atol=1e-12)
+            assert np.allclose(got[r][n], ref[n][0][:, r * Lp:(r + 1) * Lp], rtol=1e-10, atol=1e-12), (r, n)
+        assert np.allclose(got[r]["lse"], ref["lse"][0][:, r * Hp:(r + 1) * Hp], rtol=1e-12, atol=1e-12)
 
 
 @pytest.mark.parametrize("world", [2])
