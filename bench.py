@@ -44,7 +44,7 @@ METRIC = "Ulysses attn fwd+bwd TFLOP/s & % BF16 peak; relayout HBM GB/s"
 # summaries sit under profiles/). A figure is reported only while the kernel sources still
 # hash to the value recorded with it; after any change it reads as null until re-captured.
 NCU_TRAFFIC = {
-    "attn_bwd_kernel": {"bytes": 2645448192, "workload": "gpt7b", "sha": "881321f88a752b82",
+    "attn_bwd_kernel": {"bytes": 2691828764, "workload": "gpt7b", "sha": "3e1312d6d0eeaefc",
                         "sources": ["ulysses_sequence_gb300/csrc/attn_bwd.cu", "ulysses_sequence_gb300/csrc/common.cuh"]},
     "attn_fwd_kernel": {"bytes": 1060478208, "workload": "gpt7b", "sha": "9da78dea16979901",
                         "sources": ["ulysses_sequence_gb300/csrc/attn_fwd.cu", "ulysses_sequence_gb300/csrc/common.cuh"]},
@@ -585,11 +585,11 @@ def main():
                    "bwd_tflops": f_bwd / (ubwd_ms * 1e-3) / 1e12 if w.backward else None,
                    "fwd_bwd_tflops": ((f_fwd + f_bwd) / ((ufwd_ms + ubwd_ms) * 1e-3) / 1e12
                                       if w.backward else None),
-                   # fwd: one attention per block pair + one merge per query block; bwd: one
+                   # fwd: one attention per block pair (the merge is in its epilogue); bwd: one
                    # backward per pair + Delta prep and dQ conversion per query block
-                   "launches_per_step": pairs_fwd + P_ring + ((pairs_fwd + 2 * P_ring) if w.backward else 0),
-                   "note": "same tensors and mask, P > H; block-pair attention + merge (fwd), "
-                           "block-pair backward + fp32 gradient sums (bwd); not part of the step"}
+                   "launches_per_step": pairs_fwd + ((pairs_fwd + 2 * P_ring) if w.backward else 0),
+                   "note": "same tensors and mask, P > H; block-pair attention merged in fp32 in its "
+                           "epilogue (fwd), block-pair backward + fp32 gradient sums (bwd); not part of the step"}
             del uo, ulse, udq, udk, udv, uws
 
     # ---- dominant launch group: the backward call (Delta prep + main + dQ convert)

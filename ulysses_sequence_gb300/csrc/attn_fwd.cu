@@ -28,6 +28,8 @@
 // operations of one thread complete in order: when S_t of a key tile is complete, the
 // previous PV_t (which read P_t from the same columns) is too, so O_t may be rescaled and
 // the columns reused without a further wait.
+#include <type_traits>
+
 #include "common.cuh"
 #include "ulysses_internal.h"
 
@@ -47,6 +49,16 @@ struct FwdParams {
     const int32_t* kcols;
     uint32_t* err;
 };
+
+// The accumulating kernels' parameters (the Ulysses-ring hybrid's block pairs): a separate
+// type, so that the plain kernel's parameters stay as they are.
+struct FwdAccParams : FwdParams {
+    float* o_acc;    // fp32 running O of the query block (layout of O)
+    float* lse_acc;  // running lse (layout of lse)
+    int mode;        // 1 store this pair's (O, lse); 2 merge into the running pair; 3 merge, write O and lse
+};
+template <bool ACC>
+using FwdParamsOf = typename std::conditional<ACC, FwdAccParams, FwdParams>::type;
 
 template <int D>
 struct FwdCfg {
@@ -137,10 +149,12 @@ struct PairSeq {
     }
 };
 
-template <int D, int MASK>
+// ACC: the epilogue merges this launch's normalised (O, lse) into an fp32 running pair
+// (the online-softmax merge of the Ulysses-ring hybrid's block pairs) instead of storing it
+template <int D, int MASK, bool ACC>
 __global__ void __launch_bounds__(320, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                const __grid_constant__ CUtensorMap tm_v, const FwdParamsOf<ACC> p) {
     using C = FwdCfg<D>;
     constexpr int NSK = C::NSK;
     constexpr int NSV = C::NSV;
@@ -419,15 +433,37 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const bool valid = s_row < p.L;
             const bool any_key = l_sum > 0.f;
             const float inv_l = any_key ? 1.0f / l_sum : 0.f;
-            __nv_bfloat16* orow;
+            size_t orow_off;
             if (p.layout == ULYSSES_LAYOUT_TOKEN_SHARDED) {
                 const int r = s_row / p.Lp, tt = s_row % p.Lp;
-                orow = static_cast<__nv_bfloat16*>(p.o) + ((size_t(r) * p.B + b) * p.Lp + tt) * size_t(p.H) * D +
-                       size_t(h) * D;
+                orow_off = ((size_t(r) * p.B + b) * p.Lp + tt) * size_t(p.H) * D + size_t(h) * D;
             } else {
                 const int g = h / p.Hp, j = h % p.Hp;
-                orow = static_cast<__nv_bfloat16*>(p.o) + ((size_t(g) * p.B + b) * p.L + s_row) * size_t(p.Hp) * D +
-                       size_t(j) * D;
+                orow_off = ((size_t(g) * p.B + b) * p.L + s_row) * size_t(p.Hp) * D + size_t(j) * D;
+            }
+            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + orow_off;
+            const size_t li = ((size_t(h / p.Hp) * p.B + b) * p.Hp + (h % p.Hp)) * p.L + s_row;
+            float lse = any_key ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+            // ACC: this pair's part gets weight w_new, the running part w_run (lse = ln sum exp)
+            float w_run = 0.f, w_new = 1.f;
+            int mode = 0;
+            float* arow = nullptr;
+            if constexpr (ACC) {
+                mode = p.mode;
+                arow = p.o_acc + orow_off;
+                if (mode >= 2 && valid) {
+                    const float lr = p.lse_acc[li];
+                    const float mx = fmaxf(lr, lse);
+                    if (mx == -INFINITY) {
+                        w_new = 0.f;
+                    } else {
+                        const float er = __expf(lr - mx), en = __expf(lse - mx);
+                        const float tot = er + en;
+                        w_run = er / tot;
+                        w_new = en / tot;
+                        lse = mx + __logf(tot);
+                    }
+                }
             }
 #pragma unroll
             for (int i = 0; i < D / 32; ++i) {
@@ -438,19 +474,38 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
 #pragma unroll
                 for (int x = 0; x < 32; ++x) o[x] = (list.n > 0) ? o[x] * inv_l : 0.f;
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + i * 32);
+                if (!valid) continue;
+                if (ACC && mode != 0) {
+                    float4* a4 = reinterpret_cast<float4*>(arow + i * 32);
+                    if (mode >= 2) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        dst[v] = make_uint4(pack_bf16(o[8 * v + 0], o[8 * v + 1]), pack_bf16(o[8 * v + 2], o[8 * v + 3]),
-                                            pack_bf16(o[8 * v + 4], o[8 * v + 5]), pack_bf16(o[8 * v + 6], o[8 * v + 7]));
+                        for (int y = 0; y < 8; ++y) {
+                            const float4 t = a4[y];
+                            o[4 * y] = w_run * t.x + w_new * o[4 * y];
+                            o[4 * y + 1] = w_run * t.y + w_new * o[4 * y + 1];
+                            o[4 * y + 2] = w_run * t.z + w_new * o[4 * y + 2];
+                            o[4 * y + 3] = w_run * t.w + w_new * o[4 * y + 3];
+                        }
                     }
+                    if (mode <= 2) {
+#pragma unroll
+                        for (int y = 0; y < 8; ++y) a4[y] = make_float4(o[4 * y], o[4 * y + 1], o[4 * y + 2], o[4 * y + 3]);
+                        continue;
+                    }
+                }
+                uint4* dst = reinterpret_cast<uint4*>(orow + i * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    dst[v] = make_uint4(pack_bf16(o[8 * v + 0], o[8 * v + 1]), pack_bf16(o[8 * v + 2], o[8 * v + 3]),
+                                        pack_bf16(o[8 * v + 4], o[8 * v + 5]), pack_bf16(o[8 * v + 6], o[8 * v + 7]));
                 }
             }
             if (valid) {
-                const int g = h / p.Hp, j = h % p.Hp;
-                const float lse = any_key ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
-                p.lse[((size_t(g) * p.B + b) * p.Hp + j) * p.L + s_row] = lse;
+                if (ACC && mode != 0 && mode <= 2) {
+                    if constexpr (ACC) p.lse_acc[li] = lse;
+                } else {
+                    p.lse[li] = lse;
+                }
             }
         }
     }
@@ -464,19 +519,38 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-template <int D, int MASK>
-static int launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const FwdParams& p,
-                        cudaStream_t stream) {
+template <int D, int MASK, bool ACC>
+static int launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                        const FwdParamsOf<ACC>& p, cudaStream_t stream) {
     using C = FwdCfg<D>;
-    auto kern = attn_fwd_kernel<D, MASK>;
+    auto kern = attn_fwd_kernel<D, MASK, ACC>;
     if (!set_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return ULYSSES_ERR_CUDA;
     dim3 grid(p.n_pairs, p.B * p.H);
     kern<<<grid, C::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }
 
+template <int D>
+static int launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const FwdParams& p,
+                        int kind, const FwdChain& chain, cudaStream_t stream) {
+    if (chain.mode != 0) {
+        FwdAccParams ap;
+        static_cast<FwdParams&>(ap) = p;
+        ap.o_acc = chain.o_acc;
+        ap.lse_acc = chain.lse_acc;
+        ap.mode = chain.mode;
+        // the accumulating epilogue is built for the masks of the ring blocks only
+        if (kind == ULYSSES_MASK_CAUSAL) return launch_fwd_t<D, ULYSSES_MASK_CAUSAL, true>(mq, mk, mv, ap, stream);
+        if (kind == ULYSSES_MASK_NONE) return launch_fwd_t<D, ULYSSES_MASK_NONE, true>(mq, mk, mv, ap, stream);
+        return ULYSSES_ERR_UNSUPPORTED;
+    }
+    if (kind == ULYSSES_MASK_CAUSAL) return launch_fwd_t<D, ULYSSES_MASK_CAUSAL, false>(mq, mk, mv, p, stream);
+    if (kind == ULYSSES_MASK_NONE) return launch_fwd_t<D, ULYSSES_MASK_NONE, false>(mq, mk, mv, p, stream);
+    return launch_fwd_t<D, ULYSSES_MASK_BLOCK_SPARSE, false>(mq, mk, mv, p, stream);
+}
+
 int launch_attn_fwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, int layout, const void* q,
-                    const void* k, const void* v, void* o, float* lse, cudaStream_t stream) {
+                    const void* k, const void* v, void* o, float* lse, cudaStream_t stream, const FwdChain& chain) {
     FwdParams p{};
     p.B = s.B; p.L = s.L; p.H = s.H; p.P = s.P; p.Hp = s.H / s.P; p.Lp = s.L / s.P;
     const KvInfo kv = kv_info(s);
@@ -498,14 +572,10 @@ int launch_attn_fwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, in
         !encode_qkv_map(&mk, k, s, layout, p.box_rows, kv.Hkv, kv.Hkvp) ||
         !encode_qkv_map(&mv, v, s, layout, p.box_rows, kv.Hkv, kv.Hkvp))
         return ULYSSES_ERR_CUDA;
-    if (s.d_h == 128) {
-        if (m.kind == ULYSSES_MASK_CAUSAL) return launch_fwd_t<128, ULYSSES_MASK_CAUSAL>(mq, mk, mv, p, stream);
-        if (m.kind == ULYSSES_MASK_NONE) return launch_fwd_t<128, ULYSSES_MASK_NONE>(mq, mk, mv, p, stream);
-        return launch_fwd_t<128, ULYSSES_MASK_BLOCK_SPARSE>(mq, mk, mv, p, stream);
-    }
-    if (m.kind == ULYSSES_MASK_CAUSAL) return launch_fwd_t<64, ULYSSES_MASK_CAUSAL>(mq, mk, mv, p, stream);
-    if (m.kind == ULYSSES_MASK_NONE) return launch_fwd_t<64, ULYSSES_MASK_NONE>(mq, mk, mv, p, stream);
-    return launch_fwd_t<64, ULYSSES_MASK_BLOCK_SPARSE>(mq, mk, mv, p, stream);
+    if (chain.mode < 0 || chain.mode > 3 || (chain.mode != 0 && (!chain.o_acc || !chain.lse_acc)))
+        return ULYSSES_ERR_INVALID_ARG;
+    if (s.d_h == 128) return launch_fwd_d<128>(mq, mk, mv, p, m.kind, chain, stream);
+    return launch_fwd_d<64>(mq, mk, mv, p, m.kind, chain, stream);
 }
 
 }  // namespace ulysses

@@ -63,8 +63,19 @@ int launch_relayout(const ulysses_shape_t& s, const void* in, void* out, cudaStr
 // Key/value relayouts with replication (P > Hkv): seq->head copies, head->seq sums the copies.
 int launch_kv_replicated(const ulysses_shape_t& s, const void* in, void* out, cudaStream_t stream, bool to_head);
 
+// How one forward launch joins a chain of launches over the same query rows (the block pairs of
+// the Ulysses-ring hybrid). The default is a standalone forward.
+struct FwdChain {
+    // 0 write O (bf16) and lse; 1 store this launch's normalised O and lse to the fp32 running
+    // pair; 2 merge into the running pair (online-softmax rule); 3 merge and write O and lse
+    int mode = 0;
+    float* o_acc = nullptr;    // same layout as O, fp32
+    float* lse_acc = nullptr;  // same layout as lse
+};
+
 int launch_attn_fwd(const ulysses_shape_t& s, const MaskArgs& m, float scale, int layout, const void* q,
-                    const void* k, const void* v, void* o, float* lse, cudaStream_t stream);
+                    const void* k, const void* v, void* o, float* lse, cudaStream_t stream,
+                    const FwdChain& chain = FwdChain());
 
 // How one backward launch joins a chain of launches that add into the same gradients (the block
 // pairs of the Ulysses-ring hybrid). The default is a standalone backward.
