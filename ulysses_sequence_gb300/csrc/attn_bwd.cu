@@ -210,6 +210,35 @@ __device__ __forceinline__ size_t dq_block(const BwdParams& p, int bh, int qstep
     return ((size_t(bh) * p.n_tiles + qstep) * 2 + hq) * size_t(D / 32) + wq;
 }
 
+// The block-sparse schedule, four arrays of n_tiles ints in the workspace behind Delta:
+// order (key tiles by descending CSC length, ties by index), their lengths, and for each
+// position of order the start and size of its class (the run of equal lengths).
+__device__ __forceinline__ const int32_t* bwd_schedule(const BwdParams& p) {
+    const size_t rows = size_t(p.B) * p.H * p.L;
+    return reinterpret_cast<const int32_t*>(p.delta + (rows + 63) / 64 * 64);
+}
+
+// The key tile and key/value unit of this CTA. Block-sparse masks deal the CTAs out longest
+// first: tiles of one length class go out together, unit by unit within the class, so that the
+// long tiles (a global key tile walks every query tile) start in the first waves, and the
+// long tiles of one (batch, head) run side by side and share its Q and dO in L2.
+template <int MASK>
+__device__ __forceinline__ void bwd_cta_tile(const BwdParams& p, int units, int& kt, int& unit) {
+    if (MASK != ULYSSES_MASK_BLOCK_SPARSE) {
+        kt = blockIdx.x;
+        unit = blockIdx.y;
+        return;
+    }
+    const int32_t* sched = bwd_schedule(p);
+    const int n = p.n_tiles;
+    const int64_t i = int64_t(blockIdx.y) * n + blockIdx.x;
+    const int pos = int(i / units);
+    const int start = sched[2 * n + pos], size = sched[3 * n + pos];
+    const int64_t j = i - int64_t(start) * units;
+    unit = int(j / size);
+    kt = sched[start + int(j % size)];
+}
+
 template <int MASK>
 __device__ __forceinline__ int bwd_q_count(const BwdParams& p, int kt, int& first) {
     if (MASK == ULYSSES_MASK_CAUSAL) {
@@ -278,9 +307,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int lane = static_cast<int>(lane_id());
     // key tiles vary fastest, so the CTAs resident at one time share one head and its
     // fp32 dQ accumulator stays in L2
-    const KvUnit u = kv_unit(p, blockIdx.y);
+    int kt, unit;
+    bwd_cta_tile<MASK>(p, int(gridDim.y), kt, unit);
+    const KvUnit u = kv_unit(p, unit);
     const int b = u.b;
-    const int kt = blockIdx.x;
     int q_first = 0;
     const int n_per = bwd_q_count<MASK>(p, kt, q_first);  // query steps per query head
     const int n_it = n_per * u.nqh;                        // steps over all the unit's query heads
@@ -762,7 +792,43 @@ static size_t acc_bytes(const ulysses_shape_t& s) {
 
 size_t bwd_workspace_bytes(const ulysses_shape_t& s) {
     const size_t rows = size_t(s.B) * s.H * s.L;
-    return acc_bytes(s) + (rows * 4 + 255) / 256 * 256;
+    const size_t n_tiles = (size_t(s.L) + kTile - 1) / kTile;
+    return acc_bytes(s) + (rows * 4 + 255) / 256 * 256 + (4 * n_tiles * 4 + 255) / 256 * 256;
+}
+
+// Block-sparse schedule, step 1: each key tile's rank by (CSC length descending, index).
+__global__ void __launch_bounds__(256) bwd_order_kernel(const int32_t* colptr, int n, int32_t* sched) {
+    for (int kt = blockIdx.x * blockDim.x + threadIdx.x; kt < n; kt += gridDim.x * blockDim.x) {
+        const int len = colptr[kt + 1] - colptr[kt];
+        int rank = 0;
+        for (int j = 0; j < n; ++j) {
+            const int lj = colptr[j + 1] - colptr[j];
+            rank += (lj > len || (lj == len && j < kt)) ? 1 : 0;
+        }
+        sched[rank] = kt;
+        sched[n + rank] = len;
+    }
+}
+
+// Step 2: for each position of the order, the start and size of its run of equal lengths
+// (binary searches over the non-increasing lengths).
+__global__ void __launch_bounds__(256) bwd_class_kernel(int n, int32_t* sched) {
+    const int32_t* len = sched + n;
+    for (int pos = blockIdx.x * blockDim.x + threadIdx.x; pos < n; pos += gridDim.x * blockDim.x) {
+        const int l = len[pos];
+        int lo = 0, hi = pos;  // first index with len == l
+        while (lo < hi) {
+            const int mid = (lo + hi) / 2;
+            if (len[mid] > l) lo = mid + 1; else hi = mid;
+        }
+        int lo2 = pos, hi2 = n;  // first index with len < l
+        while (lo2 < hi2) {
+            const int mid = (lo2 + hi2) / 2;
+            if (len[mid] >= l) lo2 = mid + 1; else hi2 = mid;
+        }
+        sched[2 * n + pos] = lo;
+        sched[3 * n + pos] = lo2 - lo;
+    }
 }
 
 template <int D, int MASK, bool ACC>
@@ -796,6 +862,13 @@ static int launch_bwd_d(const ulysses_shape_t& s, const MaskArgs& m, BwdParams& 
         bwd_prep_kernel<D><<<unsigned(blocks), 256, 0, stream>>>(p, static_cast<const __nv_bfloat16*>(o),
                                                                   static_cast<const __nv_bfloat16*>(dO),
                                                                   const_cast<float*>(p.delta));
+        if (cudaGetLastError() != cudaSuccess) return ULYSSES_ERR_CUDA;
+    }
+    if (m.kind == ULYSSES_MASK_BLOCK_SPARSE) {
+        int32_t* sched = reinterpret_cast<int32_t*>(const_cast<float*>(p.delta) + (rows + 63) / 64 * 64);
+        const unsigned ob = unsigned((p.n_tiles + 255) / 256);
+        bwd_order_kernel<<<ob, 256, 0, stream>>>(p.colptr, p.n_tiles, sched);
+        bwd_class_kernel<<<ob, 256, 0, stream>>>(p.n_tiles, sched);
         if (cudaGetLastError() != cudaSuccess) return ULYSSES_ERR_CUDA;
     }
     int rc;
