@@ -752,34 +752,48 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p, const __nv_b
         acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// dQ = bf16(scale * accumulator), written in the output layout. One warp per accumulator
-// block (32 features x 64 queries): lane l reads its feature's 64 values (256 contiguous
-// bytes) and the warp writes, query by query, 32 consecutive features (64 bytes).
+// dQ = bf16(scale * accumulator), written in the output layout. One warp per (batch x head,
+// query step, query half): the D/32 accumulator blocks of those 64 queries. Thread t takes
+// features [8 o, 8 o + 8) with o = t % (D / 8) and every other 4-query unit; per unit it loads
+// its 8 features' 16-byte units, transposes them in registers and writes four 16-byte rows
+// pieces, so that the threads of one unit write whole contiguous rows.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdParams p, __nv_bfloat16* dq) {
-    constexpr int NQ = D / 32;
-    const size_t blocks = size_t(p.B) * p.H * p.n_tiles * 2 * NQ;
+    constexpr int NQ = D / 32;          // feature quadrants (blocks per group)
+    constexpr int OCT = D / 8;          // feature octets: 16 for d = 128, 8 for d = 64
+    constexpr int UPASS = 32 / OCT;     // 4-query units a warp covers at once: 2 or 4
+    const size_t groups = size_t(p.B) * p.H * p.n_tiles * 2;
     const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t sw = lane & 7u;
-    for (size_t blk = (size_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32; blk < blocks;
-         blk += size_t(gridDim.x) * blockDim.x / 32) {
-        const int wq = int(blk % NQ);
-        const int hq = int(blk / NQ % 2);
-        const size_t sb = blk / NQ / 2;  // (batch x head, query step)
+    const int o = int(lane) % OCT;
+    const int wq = o / 4;               // quadrant of this thread's features
+    const int l0 = (o % 4) * 8;         // first feature lane within the quadrant block
+    for (size_t grp = (size_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32; grp < groups;
+         grp += size_t(gridDim.x) * blockDim.x / 32) {
+        const int hq = int(grp % 2);
+        const size_t sb = grp / 2;  // (batch x head, query step)
         const int qstep = int(sb % p.n_tiles);
         const int bh = int(sb / p.n_tiles);
         const int h = bh % p.H, b = bh / p.H;
+        const float* blk = p.dq_acc + (grp * NQ + wq) * kDqBlockFloats;
         const int s0 = qstep * kQStep + hq * 64;
-        const int e = wq * 32 + int(lane);
-        const float4* src = reinterpret_cast<const float4*>(p.dq_acc + blk * kDqBlockFloats + lane * 64);
-#pragma unroll 4
-        for (int u4 = 0; u4 < 16; ++u4) {
-            const float4 x = src[uint32_t(u4) ^ sw];
-            const float xs[4] = {x.x, x.y, x.z, x.w};
+        for (int u = int(lane) / OCT; u < 16; u += UPASS) {
+            float x[8][4];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int l = l0 + i;
+                const float4 v = reinterpret_cast<const float4*>(blk + l * 64)[uint32_t(u) ^ uint32_t(l & 7)];
+                x[i][0] = v.x; x[i][1] = v.y; x[i][2] = v.z; x[i][3] = v.w;
+            }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int s = s0 + 4 * u4 + c;
-                if (s < p.L) dq[row_offset(p, s, h, b, D) + e] = __float2bfloat16_rn(xs[c] * p.scale);
+                const int s = s0 + 4 * u + c;
+                if (s >= p.L) continue;
+                uint4 w;
+                w.x = pack_bf16(x[0][c] * p.scale, x[1][c] * p.scale);
+                w.y = pack_bf16(x[2][c] * p.scale, x[3][c] * p.scale);
+                w.z = pack_bf16(x[4][c] * p.scale, x[5][c] * p.scale);
+                w.w = pack_bf16(x[6][c] * p.scale, x[7][c] * p.scale);
+                *reinterpret_cast<uint4*>(dq + row_offset(p, s, h, b, D) + 8 * o) = w;
             }
         }
     }
