@@ -11,25 +11,37 @@
 //                    attention kernels read (no relayout pass);
 //   out projection:  A = O [M][H d], B = W_o [hidden][H d], C = Y [M][hidden].
 //
-// A persistent CTA per SM walks 128 x 256 tiles of C on the 5th-generation tensor cores:
-// warp 0 loads A and B K-slices of 64 through a 4-stage TMA ring that runs on across tiles,
-// warp 1 issues M128 N256 K16 MMAs into one of two TMEM accumulators (256 columns each),
-// warps 2-5 convert the other accumulator to bf16 and store it, so a tile's epilogue
-// overlaps the next tile's MMAs. Tiles are rasterized in groups of 8 row tiles, so the
-// tiles in flight at one time share their A and B slices in L2.
+// Persistent CTA pairs (clusters of two on neighbouring SMs) walk 256 x 256 tiles of C on the
+// 5th-generation tensor cores with paired-SM MMAs (tcgen05 cta_group::2): each CTA holds 128
+// rows of A and its 128-row half of B, and the pair's M256 N256 K16 MMA, issued by the
+// leader, reads both CTAs' shared memory and writes each CTA's 128 rows into its own tensor
+// memory. Per SM that halves the B operand's loads and shared-memory reads against a 1-SM
+// 128 x 256 tile, whose traffic (about 190 B/clk) exceeded the 128 B/clk shared-memory port.
+//   warp 0 (both CTAs) loads A and B K-slices of 64 through a 6-stage TMA ring that runs on
+//          across tiles; both CTAs' loads count on the leader's barrier;
+//   warp 1 (leader) issues the MMAs into one of two TMEM accumulators (256 columns each) and
+//          commits to the barriers of both CTAs at once;
+//   warps 2-5 (both CTAs) convert the other accumulator to bf16 and store their rows, so a
+//          tile's epilogue overlaps the next tile's MMAs.
+// Tiles are rasterized in groups of 8 row tiles, so the tiles in flight at one time share
+// their A and B slices in L2.
+#include <mutex>
+
 #include "common.cuh"
 #include "ulysses_internal.h"
 
 namespace ulysses {
 
 struct GemmCfg {
-    static constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, GROUP_M = 8;
+    // a CTA pair computes a 256 x 256 tile; each CTA holds 128 rows of A and 128 rows of B
+    static constexpr int BM = 128, BN = 256, BK = 64, STAGES = 6, GROUP_M = 8;
+    static constexpr int PM = 2 * BM;                  // pair tile rows
     static constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
-    static constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
+    static constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's half of B
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t OFF_BAR = STAGES * STAGE_BYTES;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
-    static constexpr uint32_t TMEM_COLS = 512;  // two accumulators
+    static constexpr uint32_t TMEM_COLS = 512;  // two accumulators of 256 columns
     static constexpr int kThreads = 192;
 };
 
@@ -42,23 +54,25 @@ struct GemmParams {
     uint32_t* err;
 };
 
-__global__ void __launch_bounds__(GemmCfg::kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg::kThreads, 1)
 proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, const GemmParams p) {
     using C = GemmCfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    uint64_t* full = bars;                  // [STAGES]
-    uint64_t* empty = bars + C::STAGES;     // [STAGES]
-    uint64_t* acc_full = bars + 2 * C::STAGES;   // [2]
-    uint64_t* acc_empty = acc_full + 2;          // [2], 4 epilogue warps
+    uint64_t* full = bars;                  // [STAGES], the leader's counts both CTAs' loads
+    uint64_t* empty = bars + C::STAGES;     // [STAGES], both CTAs (multicast commit)
+    uint64_t* acc_full = bars + 2 * C::STAGES;   // [2], both CTAs (multicast commit)
+    uint64_t* acc_empty = acc_full + 2;          // [2], the leader's: 4 epilogue warps of each CTA
     uint64_t* drain = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = static_cast<int>(warp_id());
     const int lane = static_cast<int>(lane_id());
-    const int tiles_m = (p.M + C::BM - 1) / C::BM, tiles_n = (p.N + C::BN - 1) / C::BN;
+    const uint32_t rank = cluster_rank();    // 0: the leader, which issues the pair's MMAs
+    const int pair = blockIdx.x / 2, n_pairs = gridDim.x / 2;
+    const int tiles_m = (p.M + C::PM - 1) / C::PM, tiles_n = (p.N + C::BN - 1) / C::BN;
     const int n_tiles = tiles_m * tiles_n;
     const int n_k = (p.K + C::BK - 1) / C::BK;
     // grouped raster: GROUP_M row tiles vary fastest, then column tiles, then groups
@@ -67,7 +81,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         const int group = t / per_group;
         const int gm = min(C::GROUP_M, tiles_m - group * C::GROUP_M);  // row tiles in this group
         const int in_group = t - group * per_group;
-        m0 = (group * C::GROUP_M + in_group % gm) * C::BM;
+        m0 = (group * C::GROUP_M + in_group % gm) * C::PM;
         n0 = (in_group / gm) * C::BN;
     };
 
@@ -78,91 +92,99 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(acc_full + i, 1);
-            mbar_init(acc_empty + i, 4);
+            mbar_init(acc_empty + i, 8);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+    if (warp == 1) tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
     tc_fence_before();
-    __syncthreads();
+    // both CTAs' barriers exist before either CTA signals the other's
+    cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Abort ab{abort_flag, p.err, KID_PROJ};
 
     if (warp == 0) {
-        // ------------------------------------------------------------------ producer
+        // ------------------------------------------------------------------ producer (both CTAs)
         if (lane == 0) {
             tma_prefetch_desc(&tm_a);
             tma_prefetch_desc(&tm_b);
-            int issued = 0;  // K-slices loaded so far, over all of this CTA's tiles
+            int issued = 0;  // K-slices loaded so far, over all of this pair's tiles
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+            for (int t = pair; ok && t < n_tiles; t += n_pairs) {
                 int m0, n0;
                 tile_origin(t, m0, n0);
                 for (int ks = 0; ks < n_k; ++ks, ++issued) {
                     const int s = issued % C::STAGES;
                     if (issued >= C::STAGES &&
-                        !(ok = mbar_wait(empty + s, ((issued / C::STAGES) - 1) & 1, ab, ROLE_LOAD, 1)))
+                        !(ok = mbar_wait_cl(empty + s, ((issued / C::STAGES) - 1) & 1, ab, ROLE_LOAD, 1)))
                         break;
                     uint8_t* st = smem + s * C::STAGE_BYTES;
-                    mbar_arrive_expect_tx(full + s, C::STAGE_BYTES);
-                    tma_load_2d(st, &tm_a, full + s, ks * C::BK, m0);
-                    tma_load_2d(st + C::A_BYTES, &tm_b, full + s, ks * C::BK, n0);
+                    // both CTAs' bytes count on the leader's barrier; the leader expects them all
+                    if (rank == 0) mbar_arrive_expect_tx(full + s, 2 * C::STAGE_BYTES);
+                    const uint32_t lbar = cluster_addr(full + s, 0);
+                    tma_load_2d_pair(st, &tm_a, lbar, ks * C::BK, m0 + int(rank) * C::BM);
+                    tma_load_2d_pair(st + C::A_BYTES, &tm_b, lbar, ks * C::BK, n0 + int(rank) * (C::BN / 2));
                 }
             }
             if (!ok) {
-                for (int s = 0; s < C::STAGES; ++s) {
-                    const int cnt = issued > s ? (issued - 1 - s) / C::STAGES + 1 : 0;
-                    if (cnt > 0) mbar_drain(full + s, (cnt - 1) & 1);
+                // wait (bounded) for this CTA's stages' last loads to land: the leader's barrier
+                // tracks them, so only the leader can; the peer waits on its empty barriers
+                if (rank == 0) {
+                    for (int s = 0; s < C::STAGES; ++s) {
+                        const int cnt = issued > s ? (issued - 1 - s) / C::STAGES + 1 : 0;
+                        if (cnt > 0) mbar_drain(full + s, (cnt - 1) & 1);
+                    }
                 }
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(C::BM, C::BN, 0, 0);
+        // ------------------------------------------------------------------ MMA issuer (leader)
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = idesc_bf16(C::PM, C::BN, 0, 0);
             const uint32_t base = smem_u32(smem);
             bool ok = true;
             int used = 0;  // K-slices consumed so far
-            for (int t = blockIdx.x, i = 0; ok && t < n_tiles; t += gridDim.x, ++i) {
+            for (int t = pair, i = 0; ok && t < n_tiles; t += n_pairs, ++i) {
                 const int a = i & 1;
-                // the epilogue must have read this accumulator's previous tile
-                if (i >= 2 && !(ok = mbar_wait(acc_empty + a, ((i >> 1) - 1) & 1, ab, ROLE_MMA, 2))) break;
+                // both CTAs' epilogues must have read this accumulator's previous tile
+                if (i >= 2 && !(ok = mbar_wait_cl(acc_empty + a, ((i >> 1) - 1) & 1, ab, ROLE_MMA, 2))) break;
                 tc_fence_after();
                 const uint32_t acc = tmem + a * C::BN;
                 for (int ks = 0; ks < n_k; ++ks, ++used) {
                     const int s = used % C::STAGES;
-                    if (!(ok = mbar_wait(full + s, (used / C::STAGES) & 1, ab, ROLE_MMA, 1))) break;
+                    if (!(ok = mbar_wait_cl(full + s, (used / C::STAGES) & 1, ab, ROLE_MMA, 1))) break;
                     tc_fence_after();
                     const uint64_t da = sdesc_sw128(base + s * C::STAGE_BYTES, 16, 1024);
                     const uint64_t db = sdesc_sw128(base + s * C::STAGE_BYTES + C::A_BYTES, 16, 1024);
 #pragma unroll
                     for (int k = 0; k < C::BK / 16; ++k)
-                        umma_ss(acc, sdesc_add(da, k * 32), sdesc_add(db, k * 32), idesc, (ks > 0 || k > 0) ? 1u : 0u);
-                    umma_commit(empty + s);
+                        umma_pair_ss(acc, sdesc_add(da, k * 32), sdesc_add(db, k * 32), idesc, (ks > 0 || k > 0) ? 1u : 0u);
+                    umma_pair_commit_both(empty + s);
                 }
-                if (ok) umma_commit(acc_full + a);
+                if (ok) umma_pair_commit_both(acc_full + a);
             }
             if (!ok) {
-                umma_commit(drain);
+                umma_pair_commit_both(drain);
                 mbar_drain(drain, 0);
             }
         }
     } else {
-        // ------------------------------------------------------------------ epilogue
-        // thread = one row of the tile (TMEM lane); 32-column chunks go to the output that
-        // holds them (the column ranges are multiples of 32 wide)
+        // ------------------------------------------------------------------ epilogue (both CTAs)
+        // thread = one row of this CTA's 128 rows of the pair tile (TMEM lane); 32-column
+        // chunks go to the output that holds them (the column ranges are multiples of 32 wide)
         const int wq = warp & 3;
         const uint32_t lane_off = uint32_t(wq * 32) << 16;
-        for (int t = blockIdx.x, i = 0; n_k > 0 && t < n_tiles; t += gridDim.x, ++i) {
+        const uint32_t lacc_empty0 = cluster_addr(acc_empty, 0);
+        for (int t = pair, i = 0; n_k > 0 && t < n_tiles; t += n_pairs, ++i) {
             const int a = i & 1;
             int m0, n0;
             tile_origin(t, m0, n0);
-            if (!__all_sync(0xffffffffu, mbar_wait(acc_full + a, (i >> 1) & 1, ab, ROLE_EPI, 1))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait_cl(acc_full + a, (i >> 1) & 1, ab, ROLE_EPI, 1))) break;
             tc_fence_after();
-            const int row = m0 + wq * 32 + lane;
+            const int row = m0 + int(rank) * C::BM + wq * 32 + lane;
             const uint32_t acc = tmem + lane_off + a * C::BN;
 #pragma unroll 1
             for (int c = 0; c < C::BN; c += 32) {
@@ -182,19 +204,20 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                                            pack_bf16(v[8 * x + 4], v[8 * x + 5]), pack_bf16(v[8 * x + 6], v[8 * x + 7]));
                 }
             }
-            // this accumulator may take the next tile but one
+            // this accumulator may take the next tile but one (the leader counts both CTAs)
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty + a);
+            if (lane == 0) mbar_arrive_cluster(lacc_empty0 + uint32_t(a) * 8u);
         }
     }
 
     tc_fence_before();
     __syncwarp();
-    __syncthreads();
+    // the pair's MMAs and both CTAs' TMEM reads are over before either CTA frees the columns
+    cluster_sync_all();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
+        tmem_dealloc_pair(tmem, C::TMEM_COLS);
     }
 }
 
@@ -218,12 +241,33 @@ int launch_proj_gemm(int M, int N, int K, const void* a, const void* b, int n_ou
     p.err = device_error_word();
     if (!p.err) return ULYSSES_ERR_CUDA;
     CUtensorMap ma, mb;
-    if (!encode_2d(&ma, a, uint64_t(M), uint64_t(K), C::BM) || !encode_2d(&mb, b, uint64_t(N), uint64_t(K), C::BN))
+    // each CTA of a pair loads 128 rows of A and 128 rows (its half) of B per K-slice
+    if (!encode_2d(&ma, a, uint64_t(M), uint64_t(K), C::BM) || !encode_2d(&mb, b, uint64_t(N), uint64_t(K), C::BN / 2))
         return ULYSSES_ERR_CUDA;
     if (!set_max_dynamic_smem(reinterpret_cast<const void*>(proj_gemm_kernel), C::SMEM_BYTES)) return ULYSSES_ERR_CUDA;
-    const int tiles = ((M + C::BM - 1) / C::BM) * ((N + C::BN - 1) / C::BN);
-    const int grid = tiles < device_sm_count() ? tiles : device_sm_count();  // persistent: one CTA per SM
-    proj_gemm_kernel<<<grid, C::kThreads, C::SMEM_BYTES, stream>>>(ma, mb, p);
+    const int tiles = ((M + C::PM - 1) / C::PM) * ((N + C::BN - 1) / C::BN);
+    // persistent: as many CTA pairs as can be resident at once (a pair needs two SMs of one
+    // cluster-capable group; asked of the runtime once per device)
+    static std::mutex mu;
+    static int resident[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ULYSSES_ERR_CUDA;
+    int pairs;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (resident[dev] == 0) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(unsigned(device_sm_count() / 2 * 2));
+            cfg.blockDim = dim3(C::kThreads);
+            cfg.dynamicSmemBytes = C::SMEM_BYTES;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, proj_gemm_kernel, &cfg) != cudaSuccess || n <= 0) return ULYSSES_ERR_CUDA;
+            resident[dev] = n;
+        }
+        pairs = resident[dev];
+    }
+    if (tiles < pairs) pairs = tiles;
+    proj_gemm_kernel<<<2 * pairs, C::kThreads, C::SMEM_BYTES, stream>>>(ma, mb, p);
     return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }
 
