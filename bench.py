@@ -44,9 +44,9 @@ METRIC = "Ulysses attn fwd+bwd TFLOP/s & % BF16 peak; relayout HBM GB/s"
 # summaries sit under profiles/). A figure is reported only while the kernel sources still
 # hash to the value recorded with it; after any change it reads as null until re-captured.
 NCU_TRAFFIC = {
-    "attn_bwd_kernel": {"bytes": 2691828764, "workload": "gpt7b", "sha": "3e1312d6d0eeaefc",
+    "attn_bwd_kernel": {"bytes": 2691430172, "workload": "gpt7b", "sha": "d955a1f9c6224abd",
                         "sources": ["ulysses_sequence_gb300/csrc/attn_bwd.cu", "ulysses_sequence_gb300/csrc/common.cuh"]},
-    "attn_fwd_kernel": {"bytes": 1060478208, "workload": "gpt7b", "sha": "9da78dea16979901",
+    "attn_fwd_kernel": {"bytes": 1057295303, "workload": "gpt7b", "sha": "32ffcfe50651b16e",
                         "sources": ["ulysses_sequence_gb300/csrc/attn_fwd.cu", "ulysses_sequence_gb300/csrc/common.cuh"]},
 }
 
@@ -163,6 +163,8 @@ def dist_setup(force: bool = False):
     if world > 1 or force:
         import torch.distributed as dist
         backend = "nccl" if torch.cuda.is_available() else "gloo"
+        # keep stdout to rank 0's one JSON line (NCCL's version banner goes there otherwise)
+        os.environ.setdefault("NCCL_DEBUG", "WARN")
         if world == 1:
             os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
             os.environ.setdefault("MASTER_PORT", "29511")
@@ -577,10 +579,19 @@ def main():
         out_call()
     qkv_ms = cuda_events_time(qkv_call, stream, 10)
     out_ms = cuda_events_time(out_call, stream, 10)
+    # cuBLAS on the same bf16 operands, timed beside them as the library-GEMM comparison
+    x2d, o2d = xs.reshape(-1, hidden), o.reshape(-1, w.H * w.d)
+    cb_qkv = lambda: torch.matmul(x2d, w_qkv.t())  # noqa: E731
+    cb_out = lambda: torch.matmul(o2d, w_o.t())  # noqa: E731
+    for _ in range(3):
+        cb_qkv()
+        cb_out()
+    cb_qkv_ms = cuda_events_time(cb_qkv, stream, 10)
+    cb_out_ms = cuda_events_time(cb_out, stream, 10)
     rows = w.B * w.L
     qkv_flops = 2 * rows * (w.H + 2 * w.Hkv) * w.d * hidden
     out_flops = 2 * rows * hidden * w.H * w.d
-    del xs, w_qkv, w_o, pq, pk, pv, py
+    del xs, w_qkv, w_o, pq, pk, pv, py, x2d, o2d
 
     # ---- the Ulysses-ring hybrid on the same tensors: P = 2H shards (beyond the head cut's
     # P <= H) as P_ring = 2 ring blocks of P_u = H shards; the same attention, so the same flops
@@ -686,6 +697,8 @@ def main():
                          "ms": rl_ms, "bytes": rl_bytes, "frac_of_measured_hbm": rl_bytes / (rl_ms * 1e-3) / 1e9 / peak_gbs},
             "projections": {"qkv_tflops": qkv_flops / (qkv_ms * 1e-3) / 1e12, "qkv_ms": qkv_ms,
                             "out_tflops": out_flops / (out_ms * 1e-3) / 1e12, "out_ms": out_ms,
+                            "cublas_qkv_tflops": qkv_flops / (cb_qkv_ms * 1e-3) / 1e12,
+                            "cublas_out_tflops": out_flops / (cb_out_ms * 1e-3) / 1e12,
                             "qkv_frac": qkv_flops / (qkv_ms * 1e-3) / 1e12 / peak_tf,
                             "out_frac": out_flops / (out_ms * 1e-3) / 1e12 / peak_tf,
                             "note": "x [B*L][H*d_h] -> Q, K, V token-sharded; O -> y; not part of the step"},
