@@ -249,8 +249,12 @@ int ulysses_out_proj(ulysses_shape_t shape, int hidden, const void *o, const voi
  * ring block must be a valid ulysses_attn_fwd shape. workspace: at least
  * ulysses_usp_workspace_size(shape, P_ring) bytes, 256-byte aligned (0 for invalid shapes). The
  * forward merges each query block's pairs into an fp32 running (O, lse) and rounds O to bf16
- * once. The backward sums partial gradients over block pairs in fp32, so all its outputs are
- * deterministic up to the reduction order of each block pair's dQ. */
+ * once. With a causal mask it runs the first query block (a single pair) on a second stream
+ * that the library keeps for each host thread and device. That stream waits for `stream` at
+ * the start of the call, and `stream` waits for it at the end through an event, so the call
+ * keeps stream order like every other call. The backward sums partial gradients over block
+ * pairs in fp32, so all its outputs are deterministic up to the reduction order of each block
+ * pair's dQ. */
 size_t ulysses_usp_workspace_size(ulysses_shape_t shape, int P_ring);
 int ulysses_usp_attn_fwd(ulysses_shape_t shape, int P_ring, const ulysses_mask_t *mask, float softmax_scale,
                          const void *q, const void *k, const void *v, void *o, float *lse, void *workspace,

@@ -42,6 +42,38 @@ UspGeom usp_geom(const ulysses_shape_t& s, int P_ring) {
     return g;
 }
 
+// A second stream of this host thread on the current device, and two events, for the forward's
+// query block that needs no running pair. They are made once per thread and device and never
+// shared, so neither another thread's work nor another thread's stream capture can interleave
+// with this thread's calls on them.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+bool side_stream(SideStream& out) {
+    constexpr int kDevs = 64;
+    thread_local SideStream side[kDevs];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return false;
+    SideStream& s = side[dev];
+    if (!s.stream) {
+        if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess) {
+            s.stream = nullptr;
+            return false;
+        }
+        if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) {
+            if (s.fork) cudaEventDestroy(s.fork);
+            cudaStreamDestroy(s.stream);
+            s = SideStream();
+            return false;
+        }
+    }
+    out = s;
+    return true;
+}
+
 }  // namespace
 
 size_t usp_workspace_bytes(const ulysses_shape_t& s, int P_ring) {
@@ -66,23 +98,43 @@ int launch_usp_fwd(const ulysses_shape_t& s, int P_ring, const MaskArgs& m, floa
     const __nv_bfloat16* k16 = static_cast<const __nv_bfloat16*>(k);
     const __nv_bfloat16* v16 = static_cast<const __nv_bfloat16*>(v);
     __nv_bfloat16* o16 = static_cast<__nv_bfloat16*>(o);
-    // Query blocks outer, key blocks inner: a query block's pairs run back to back, merging into
-    // the one running pair (stream order keeps each merge after the previous pair's).
-    for (int i = 0; i < P_ring; ++i) {
+    auto pair = [&](int i, int j, cudaStream_t st) {
         const int nj = causal ? i + 1 : P_ring;
-        for (int j = 0; j < nj; ++j) {
-            const MaskArgs& mj = (causal && j == i) ? m : none;
-            FwdChain ch;
-            ch.mode = nj == 1 ? 0 : (j == 0 ? 1 : (j + 1 == nj ? 3 : 2));
-            ch.o_acc = acc_o;
-            ch.lse_acc = acc_lse;
-            int rc = launch_attn_fwd(g.sub, mj, scale, ULYSSES_LAYOUT_TOKEN_SHARDED, q16 + i * g.q_elems,
-                                     k16 + j * g.kv_elems, v16 + j * g.kv_elems, o16 + i * g.q_elems,
-                                     lse + i * g.lse_elems, stream, ch);
-            if (rc != ULYSSES_OK) return rc;
+        const MaskArgs& mj = (causal && j == i) ? m : none;
+        FwdChain ch;
+        ch.mode = nj == 1 ? 0 : (j == 0 ? 1 : (j + 1 == nj ? 3 : 2));
+        ch.o_acc = acc_o;
+        ch.lse_acc = acc_lse;
+        return launch_attn_fwd(g.sub, mj, scale, ULYSSES_LAYOUT_TOKEN_SHARDED, q16 + i * g.q_elems, k16 + j * g.kv_elems,
+                               v16 + j * g.kv_elems, o16 + i * g.q_elems, lse + i * g.lse_elems, st, ch);
+    };
+    // Query blocks outer, key blocks inner: a query block's pairs run back to back, merging into
+    // the one running pair (stream order keeps each merge after the previous pair's). With a
+    // causal mask the first query block has one pair and no running pair. It runs on a side
+    // stream beside the others, submitted after the main stream's first launch, so that the block
+    // scheduler hands out that launch's CTAs first and the side pair's CTAs fill its last waves.
+    SideStream side;
+    const bool fork = causal && P_ring > 1 && side_stream(side);
+    if (fork && (cudaEventRecord(side.fork, stream) != cudaSuccess ||
+                 cudaStreamWaitEvent(side.stream, side.fork, 0) != cudaSuccess))
+        return ULYSSES_ERR_CUDA;
+    int rc = ULYSSES_OK;
+    bool side_done = !fork;
+    for (int i = fork ? 1 : 0; rc == ULYSSES_OK && i < P_ring; ++i) {
+        const int nj = causal ? i + 1 : P_ring;
+        for (int j = 0; rc == ULYSSES_OK && j < nj; ++j) {
+            rc = pair(i, j, stream);
+            if (rc == ULYSSES_OK && !side_done) {
+                side_done = true;
+                rc = pair(0, 0, side.stream);
+            }
         }
     }
-    return ULYSSES_OK;
+    // the caller's stream waits for the side stream, on error too (a capture must be rejoined)
+    if (fork && (cudaEventRecord(side.join, side.stream) != cudaSuccess ||
+                 cudaStreamWaitEvent(stream, side.join, 0) != cudaSuccess) && rc == ULYSSES_OK)
+        rc = ULYSSES_ERR_CUDA;
+    return rc;
 }
 
 int launch_usp_bwd(const ulysses_shape_t& s, int P_ring, const MaskArgs& m, float scale, const void* q, const void* k,
