@@ -187,3 +187,40 @@ def test_usp_gpt7b_sampled_rows():
     for s in stats.values():
         s.check()
     assert lse_err <= LSE_MAX_ABS, lse_err
+
+
+def test_usp_forward_keeps_stream_order_on_a_user_stream():
+    """With a causal mask the forward runs the first query block on the library's side stream.
+    On a user stream whose earlier work writes q, k, v late (behind a queue of matmuls), the
+    side stream must wait for that work, and work queued after the call must see the side
+    stream's rows of O. Compared bit for bit with the same call on quiet inputs."""
+    B, L, H, d, P, P_ring = 1, 2048, 4, 64, 8, 2
+    t = workloads.draw(B, L, H, d, P, 11)
+    src = {n: t[n].cuda() for n in ("q", "k", "v")}
+    mask = U.Mask.causal()
+    ref_o, ref_lse = U.usp_attn_fwd(src["q"], src["k"], src["v"], P, P_ring, mask)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    buf = {n: torch.full_like(x, float("nan")) for n, x in src.items()}
+    o = torch.full_like(src["q"], float("nan"))
+    lse = torch.full_like(ref_lse, float("nan"))
+    ws = U.usp_workspace(src["q"], P, P_ring, H)
+    a = torch.randn(4096, 4096, device="cuda", dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for _ in range(30):
+            a = a @ a * 1e-2
+        for n in buf:
+            buf[n].copy_(src[n])
+        U.usp_attn_fwd(buf["q"], buf["k"], buf["v"], P, P_ring, mask, o=o, lse=lse, workspace=ws, stream=s)
+        o_after = o.clone()
+        lse_after = lse.clone()
+    s.synchronize()
+    st, word = U.device_status()
+    assert st == U.OK, hex(word)
+    assert torch.equal(_bits_t(o_after), _bits_t(ref_o))
+    assert torch.equal(lse_after, ref_lse)
+
+
+def _bits_t(x: torch.Tensor) -> torch.Tensor:
+    return x.view(torch.int16)

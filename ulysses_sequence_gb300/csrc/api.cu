@@ -83,24 +83,70 @@ uint32_t* device_error_word() {
     return g_err[dev];
 }
 
-bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
-                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
-                       const cuuint32_t* elem_strides) {
+namespace {
+
+// A tensor map is a pure function of its arguments (the address, not the memory behind it), so
+// each host thread keeps the maps it encoded most recently and hands out a copy when the same
+// arguments come again: 64 slots, direct-mapped by a hash of the arguments.
+struct MapKey {
+    uint64_t dtype, rank;
+    uint64_t base;
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5], estr[5];
+};
+struct MapSlot {
+    MapKey key;
+    CUtensorMap map;
+    bool valid;
+};
+
+bool encode_memo(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base, const cuuint64_t* dims,
+                 const cuuint64_t* strides, const cuuint32_t* box, const cuuint32_t* estr) {
+    if (rank == 0 || rank > 5) return false;
+    MapKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.dtype = uint64_t(dtype);
+    k.rank = rank;
+    k.base = reinterpret_cast<uintptr_t>(base);
+    for (uint32_t i = 0; i < rank; ++i) {
+        k.dims[i] = dims[i];
+        k.box[i] = box[i];
+        k.estr[i] = estr[i];
+        if (i + 1 < rank) k.strides[i] = strides[i];
+    }
+    uint64_t h = 1469598103934665603ull;  // FNV-1a over the key's bytes
+    const unsigned char* kb = reinterpret_cast<const unsigned char*>(&k);
+    for (size_t i = 0; i < sizeof(k); ++i) h = (h ^ kb[i]) * 1099511628211ull;
+    thread_local MapSlot slots[64];
+    MapSlot& sl = slots[(h ^ (h >> 32)) & 63];
+    if (sl.valid && std::memcmp(&sl.key, &k, sizeof(k)) == 0) {
+        *map = sl.map;
+        return true;
+    }
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!load_encode_fn()) return false;
     }
-    return g_encode(map, dtype, rank, const_cast<void*>(base), dims, strides, box, elem_strides,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (g_encode(map, dtype, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    sl.key = k;
+    sl.map = *map;
+    sl.valid = true;
+    return true;
+}
+
+}  // namespace
+
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
+                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                       const cuuint32_t* elem_strides) {
+    return encode_memo(map, dtype, rank, base, dims, strides, box, elem_strides);
 }
 
 bool encode_qkv_map(CUtensorMap* map, const void* base, const ulysses_shape_t& s, int layout, int box_rows,
                     int heads, int group_heads) {
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (!load_encode_fn()) return false;
-    }
     const uint64_t d = s.d_h, H = heads, P = s.P, B = s.B, L = s.L;
     const uint64_t Hp = group_heads, Lp = L / P;
     cuuint64_t dims[5];
@@ -116,10 +162,7 @@ bool encode_qkv_map(CUtensorMap* map, const void* base, const ulysses_shape_t& s
     strides[3] = strides[2] * dims[3];
     cuuint32_t box[5] = {64, 1, static_cast<cuuint32_t>(box_rows), 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
-                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_memo(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, estr);
 }
 
 namespace {
