@@ -28,7 +28,9 @@
  *
  * Conventions for every call below:
  *   - Ownership: the caller allocates and owns every buffer. The library allocates no
- *     device memory; its only state is a per-process error word on each device.
+ *     device memory. Its state is a per-process error word on each device and, for each host
+ *     thread, a cache of tensor maps and the USP forward's side streams; ulysses_shutdown()
+ *     releases the calling thread's part.
  *   - Pointers are device pointers unless stated. `stream` is a cudaStream_t passed as
  *     void* (NULL = the legacy default stream). Calls enqueue work and return without
  *     synchronising; a launch failure returns ULYSSES_ERR_CUDA.
@@ -290,6 +292,14 @@ int ulysses_get_device_status(void *stream, uint32_t *detail);
 
 /* Human-readable name of a status code (static storage). */
 const char *ulysses_status_string(int status);
+
+/* Releases what the library keeps for the calling host thread: the side stream and its two
+ * events on each device (made by ulysses_usp_attn_fwd), after waiting for their work, and the
+ * thread's cache of tensor maps. Other threads' state is untouched, and the library allocates
+ * no device memory of its own. Any call afterwards makes the state again as needed. Returns
+ * ULYSSES_OK, or ULYSSES_ERR_CUDA if a wait or a device switch failed (the state is released
+ * all the same). A thread that never used them makes no CUDA call here. */
+int ulysses_shutdown(void);
 
 #ifdef __cplusplus
 }

@@ -40,6 +40,13 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(U.EXPORTS) <= set(declared_functions())
 
 
+def test_shutdown_with_no_thread_state_is_ok(lib):
+    # a thread that made no side stream releases only its host-side map cache: no CUDA call,
+    # so this holds without a GPU
+    assert U.ulysses_shutdown() == U.OK
+    U.shutdown()
+
+
 def test_status_strings(lib):
     assert U.ulysses_status_string(U.OK) == "ULYSSES_OK"
     assert U.ulysses_status_string(U.ERR_DEVICE_TIMEOUT) == "ULYSSES_ERR_DEVICE_TIMEOUT"

@@ -222,5 +222,23 @@ def test_usp_forward_keeps_stream_order_on_a_user_stream():
     assert torch.equal(lse_after, ref_lse)
 
 
+def test_usp_forward_after_shutdown_remakes_its_side_stream():
+    """ulysses_shutdown releases the thread's side stream and map cache; the next call makes them
+    again and gives the same bits."""
+    B, L, H, d, P, P_ring = 1, 1024, 4, 64, 8, 2
+    t = workloads.draw(B, L, H, d, P, 12)
+    x = {n: t[n].cuda() for n in ("q", "k", "v")}
+    mask = U.Mask.causal()
+    o1, lse1 = U.usp_attn_fwd(x["q"], x["k"], x["v"], P, P_ring, mask)
+    U.shutdown()
+    o2, lse2 = U.usp_attn_fwd(x["q"], x["k"], x["v"], P, P_ring, mask)
+    U.shutdown()
+    torch.cuda.synchronize()
+    st, word = U.device_status()
+    assert st == U.OK, hex(word)
+    assert torch.equal(_bits_t(o1), _bits_t(o2))
+    assert torch.equal(lse1, lse2)
+
+
 def _bits_t(x: torch.Tensor) -> torch.Tensor:
     return x.view(torch.int16)

@@ -41,7 +41,7 @@ EXPORTS = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_kv_seq_to_head
            "ulysses_qkv_proj", "ulysses_out_proj", "ulysses_usp_workspace_size", "ulysses_usp_attn_fwd",
            "ulysses_usp_attn_bwd", "ulysses_attn_fwd", "ulysses_attn_bwd_workspace_size",
            "ulysses_attn_bwd", "ulysses_attn_bwd_noalloc", "ulysses_bsmask_build_window_global",
-           "ulysses_get_device_status", "ulysses_selftest_timeout", "ulysses_status_string")
+           "ulysses_get_device_status", "ulysses_selftest_timeout", "ulysses_status_string", "ulysses_shutdown")
 BWD_NOALLOC_SCRATCH_BYTES = 96 * 1024 * 1024  # ULYSSES_BWD_NOALLOC_SCRATCH_BYTES
 
 _lib = None
@@ -81,6 +81,7 @@ def load() -> ctypes.CDLL:
     lib.ulysses_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.ulysses_selftest_timeout.argtypes = [vp]
     lib.ulysses_status_string.argtypes = [i]
+    lib.ulysses_shutdown.argtypes = []
     lib.ulysses_status_string.restype = ctypes.c_char_p
     for name in EXPORTS:
         if name not in ("ulysses_attn_bwd_workspace_size", "ulysses_usp_workspace_size", "ulysses_status_string"):
@@ -200,6 +201,10 @@ def ulysses_selftest_timeout(stream: int) -> int:
 
 def ulysses_status_string(status: int) -> str:
     return load().ulysses_status_string(status).decode()
+
+
+def ulysses_shutdown() -> int:
+    return load().ulysses_shutdown()
 
 
 class UlyssesError(RuntimeError):
@@ -451,6 +456,11 @@ def attn_bwd(q, k, v, o, lse, do, P: int, mask: Mask, layout: int = LAYOUT_TOKEN
                            lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
                            ws.numel(), _stream(stream)), "attn_bwd")
     return dq, dk, dv
+
+
+def shutdown() -> None:
+    """Releases the calling thread's side streams and cached tensor maps (made again on demand)."""
+    check(ulysses_shutdown(), "shutdown")
 
 
 def device_status(stream=None) -> Tuple[int, int]:

@@ -99,6 +99,7 @@ struct MapSlot {
     CUtensorMap map;
     bool valid;
 };
+thread_local MapSlot t_maps[64];
 
 bool encode_memo(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base, const cuuint64_t* dims,
                  const cuuint64_t* strides, const cuuint32_t* box, const cuuint32_t* estr) {
@@ -117,8 +118,7 @@ bool encode_memo(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, con
     uint64_t h = 1469598103934665603ull;  // FNV-1a over the key's bytes
     const unsigned char* kb = reinterpret_cast<const unsigned char*>(&k);
     for (size_t i = 0; i < sizeof(k); ++i) h = (h ^ kb[i]) * 1099511628211ull;
-    thread_local MapSlot slots[64];
-    MapSlot& sl = slots[(h ^ (h >> 32)) & 63];
+    MapSlot& sl = t_maps[(h ^ (h >> 32)) & 63];
     if (sl.valid && std::memcmp(&sl.key, &k, sizeof(k)) == 0) {
         *map = sl.map;
         return true;
@@ -522,6 +522,11 @@ int ulysses_get_device_status(void* stream, uint32_t* detail) {
     if (cudaMemcpyToSymbol(g_error_word_storage, &zero, sizeof(zero)) != cudaSuccess) return ULYSSES_ERR_CUDA;
     if (detail) *detail = word;
     return word == 0 ? ULYSSES_OK : ULYSSES_ERR_DEVICE_TIMEOUT;
+}
+
+int ulysses_shutdown(void) {
+    for (MapSlot& sl : t_maps) sl.valid = false;
+    return release_side_streams() ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -98,6 +98,8 @@ size_t bwd_workspace_bytes(const ulysses_shape_t& s);
 // Ulysses-ring hybrid over P_ring ring blocks (P_ring <= kMaxRing)
 constexpr int kMaxRing = 64;
 size_t usp_workspace_bytes(const ulysses_shape_t& s, int P_ring);
+// Waits for and destroys the calling thread's side streams and their events (USP forward).
+bool release_side_streams();
 int launch_usp_fwd(const ulysses_shape_t& s, int P_ring, const MaskArgs& m, float scale, const void* q, const void* k,
                    const void* v, void* o, float* lse, void* ws, cudaStream_t stream);
 int launch_usp_bwd(const ulysses_shape_t& s, int P_ring, const MaskArgs& m, float scale, const void* q, const void* k,

@@ -51,12 +51,13 @@ struct SideStream {
     cudaEvent_t fork = nullptr, join = nullptr;
 };
 
+constexpr int kSideDevs = 64;
+thread_local SideStream t_side[kSideDevs];
+
 bool side_stream(SideStream& out) {
-    constexpr int kDevs = 64;
-    thread_local SideStream side[kDevs];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return false;
-    SideStream& s = side[dev];
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSideDevs) return false;
+    SideStream& s = t_side[dev];
     if (!s.stream) {
         if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess) {
             s.stream = nullptr;
@@ -75,6 +76,24 @@ bool side_stream(SideStream& out) {
 }
 
 }  // namespace
+
+bool release_side_streams() {
+    int cur = -1;
+    bool ok = true;
+    for (int dev = 0; dev < kSideDevs; ++dev) {
+        SideStream& s = t_side[dev];
+        if (!s.stream) continue;
+        if (cur < 0 && cudaGetDevice(&cur) != cudaSuccess) cur = 0;
+        ok = cudaSetDevice(dev) == cudaSuccess && ok;
+        ok = cudaStreamSynchronize(s.stream) == cudaSuccess && ok;
+        cudaEventDestroy(s.fork);
+        cudaEventDestroy(s.join);
+        cudaStreamDestroy(s.stream);
+        s = SideStream();
+    }
+    if (cur >= 0) ok = cudaSetDevice(cur) == cudaSuccess && ok;
+    return ok;
+}
 
 size_t usp_workspace_bytes(const ulysses_shape_t& s, int P_ring) {
     const UspGeom g = usp_geom(s, P_ring);
