@@ -28,6 +28,7 @@
 // operations of one thread complete in order: when S_t of a key tile is complete, the
 // previous PV_t (which read P_t from the same columns) is too, so O_t may be rescaled and
 // the columns reused without a further wait.
+#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -178,13 +179,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = static_cast<int>(warp_id());
     const int lane = static_cast<int>(lane_id());
-    // query-tile pairs vary fastest (heaviest causal pairs first), so the CTAs resident at
-    // one time share one head and its K, V stay in L2
-    const int bh = blockIdx.y;
+    // Query-tile pairs vary fastest. With a causal mask grid row y holds a group of G heads
+    // (G = gridDim.x / n_pairs, chosen so that their K and V fit in a quarter of L2), dealt
+    // out heaviest pair first across the group: the resident CTAs share a few heads' K, V in
+    // L2, and the light pairs of every group fill the last waves instead of a lone head's.
+    int bh = blockIdx.y, pair = blockIdx.x;
+    if (MASK == ULYSSES_MASK_CAUSAL) {
+        const int G = static_cast<int>(gridDim.x) / p.n_pairs;
+        const int Gg = min(G, p.B * p.H - static_cast<int>(blockIdx.y) * G);
+        const int r = static_cast<int>(blockIdx.x);
+        if (r >= Gg * p.n_pairs) return;  // the last group's spare CTAs (all threads leave)
+        pair = p.n_pairs - 1 - r / Gg;
+        bh = static_cast<int>(blockIdx.y) * G + r % Gg;
+    }
     const int b = bh / p.H;
     const int h = bh % p.H;
-    const int pair = (MASK == ULYSSES_MASK_CAUSAL) ? (p.n_pairs - 1 - static_cast<int>(blockIdx.x))
-                                                    : static_cast<int>(blockIdx.x);
     const int qt0 = 2 * pair;
     const bool has1 = qt0 + 1 < p.n_tiles;
 
@@ -525,7 +534,13 @@ static int launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
     using C = FwdCfg<D>;
     auto kern = attn_fwd_kernel<D, MASK, ACC>;
     if (!set_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return ULYSSES_ERR_CUDA;
-    dim3 grid(p.n_pairs, p.B * p.H);
+    const int bh = p.B * p.H;
+    int G = 1;
+    if (MASK == ULYSSES_MASK_CAUSAL) {
+        const size_t kv_head = size_t(4) * size_t(p.L) * D;  // K and V of one head, bf16
+        G = int(std::min<size_t>(size_t(bh), std::max<size_t>(1, (size_t(32) << 20) / kv_head)));
+    }
+    dim3 grid(G * p.n_pairs, (bh + G - 1) / G);
     kern<<<grid, C::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }
