@@ -46,7 +46,7 @@ METRIC = "Ulysses attn fwd+bwd TFLOP/s & % BF16 peak; relayout HBM GB/s"
 NCU_TRAFFIC = {
     "attn_bwd_kernel": {"bytes": 2691964416, "workload": "gpt7b", "sha": "141864686c293c77",
                         "sources": ["ulysses_sequence_gb300/csrc/attn_bwd.cu", "ulysses_sequence_gb300/csrc/common.cuh"]},
-    "attn_fwd_kernel": {"bytes": 1057368348, "workload": "gpt7b", "sha": "1b44b8698dd61054",
+    "attn_fwd_kernel": {"bytes": 1060603761, "workload": "gpt7b", "sha": "dc08a5dc375912d9",
                         "sources": ["ulysses_sequence_gb300/csrc/attn_fwd.cu", "ulysses_sequence_gb300/csrc/common.cuh"]},
 }
 

@@ -148,6 +148,24 @@ def test_shard_count_and_fusion_do_not_change_results():
             assert err <= 2e-2, (P, layout, err)
 
 
+def test_forward_head_groups_with_a_partial_last_group():
+    """The causal forward deals its CTAs out in groups of G heads (G from the K/V bytes per
+    head: 2 at L = 32768, d_h = 128). With 3 heads the last group is partial and its spare CTAs
+    leave at once. Every head's O and lse must equal, bit for bit, the same head run alone
+    (one head: one group, the plain order)."""
+    B, L, H, d, P = 1, 32768, 3, 128, 1
+    g = torch.Generator().manual_seed(21)
+    x = {n: torch.randn((P, B, L, H, d), generator=g).mul_(0.5).to(torch.bfloat16).cuda() for n in ("q", "k", "v")}
+    o, lse = U.attn_fwd(x["q"], x["k"], x["v"], P, U.Mask.causal())
+    for h in range(H):
+        one = {n: t[:, :, :, h:h + 1, :].contiguous() for n, t in x.items()}
+        o1, lse1 = U.attn_fwd(one["q"], one["k"], one["v"], P, U.Mask.causal())
+        assert torch.equal(o[:, :, :, h:h + 1, :].view(torch.int16), o1.view(torch.int16)), h
+        assert torch.equal(lse[:, :, h:h + 1, :], lse1), h
+    st, word = U.device_status()
+    assert st == U.OK, hex(word)
+
+
 def test_repeat_runs_are_deterministic_except_dq():
     w = workloads.Workload("rep", 1, 1024, 4, 128, 4, "causal", True, 5)
     t = {n: x.cuda() for n, x in workloads.draw_workload(w).items()}
