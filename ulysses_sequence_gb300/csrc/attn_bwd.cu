@@ -29,6 +29,7 @@
 //      memory and issues every reduction, so none of them sits in the softmax warps' loop.
 //      Fourteen warps leave 144 registers per thread.
 //   3. bwd_dq_convert: dQ = bf16(scale * accumulator) into the output layout.
+#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -239,6 +240,21 @@ __device__ __forceinline__ void bwd_cta_tile(const BwdParams& p, int units, int&
     kt = sched[start + int(j % size)];
 }
 
+// Causal grids with short sequences deal out groups of G units (G = gridDim.x / n_tiles,
+// chosen so that their Q, dO and dQ accumulator fit in a quarter of L2), longest key tile
+// first across the group, so that the light tiles of every unit fill the last waves. Returns
+// false for the last group's spare CTAs, which have no tile.
+__device__ __forceinline__ bool bwd_cta_tile_grouped(const BwdParams& p, int& kt, int& unit) {
+    const int all = p.layout == ULYSSES_LAYOUT_TOKEN_SHARDED ? p.B * p.Hkv : p.P * p.B * p.Hkvp;
+    const int G = int(gridDim.x) / p.n_tiles;
+    const int Gg = min(G, all - int(blockIdx.y) * G);
+    const int r = int(blockIdx.x);
+    if (r >= Gg * p.n_tiles) return false;
+    kt = r / Gg;
+    unit = int(blockIdx.y) * G + r % Gg;
+    return true;
+}
+
 template <int MASK>
 __device__ __forceinline__ int bwd_q_count(const BwdParams& p, int kt, int& first) {
     if (MASK == ULYSSES_MASK_CAUSAL) {
@@ -266,7 +282,7 @@ __device__ __forceinline__ uint32_t a_col(int k) { return uint32_t(8 * k + (k >=
 // Warps of the backward kernel: producer, MMA issuer, 8 softmax, 4 dQ drain
 constexpr int kBwdThreads = 14 * 32;
 
-template <int D, int MASK, bool ACC>
+template <int D, int MASK, bool ACC, bool GRP = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -308,7 +324,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // key tiles vary fastest, so the CTAs resident at one time share one head and its
     // fp32 dQ accumulator stays in L2
     int kt, unit;
-    bwd_cta_tile<MASK>(p, int(gridDim.y), kt, unit);
+    if constexpr (GRP) {
+        if (!bwd_cta_tile_grouped(p, kt, unit)) return;  // all threads of a spare CTA
+    } else {
+        bwd_cta_tile<MASK>(p, int(gridDim.y), kt, unit);
+    }
     const KvUnit u = kv_unit(p, unit);
     const int b = u.b;
     int q_first = 0;
@@ -849,11 +869,20 @@ template <int D, int MASK, bool ACC>
 static int launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
                         const BwdParamsOf<ACC>& p, cudaStream_t stream) {
     using C = BwdCfg<D>;
-    auto kern = attn_bwd_kernel<D, MASK, ACC>;
-    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return ULYSSES_ERR_CUDA;
     // one CTA per (key tile, key/value head unit): B * Hkv units token-sharded, P * B * Hkvp head-sharded
     const int units = p.layout == ULYSSES_LAYOUT_TOKEN_SHARDED ? p.B * p.Hkv : p.P * p.B * p.Hkvp;
-    dim3 grid(p.n_tiles, units);
+    int G = 1;
+    if (MASK == ULYSSES_MASK_CAUSAL) {
+        // per unit: its query heads' Q and dO (bf16) and dQ accumulator (fp32)
+        const int nqh = p.layout == ULYSSES_LAYOUT_TOKEN_SHARDED ? p.G : (p.kv_rep == 1 ? p.G : p.Hp);
+        const size_t unit_bytes = size_t(p.L) * D * 8 * size_t(nqh);
+        G = int(std::min<size_t>(size_t(units), std::max<size_t>(1, (size_t(32) << 20) / unit_bytes)));
+    }
+    // the grouped order is a kernel of its own: the plain kernel's code stays as it is (the
+    // backward measurably slowed when its mapping code grew)
+    auto kern = G > 1 ? attn_bwd_kernel<D, MASK, ACC, true> : attn_bwd_kernel<D, MASK, ACC, false>;
+    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return ULYSSES_ERR_CUDA;
+    dim3 grid(G * p.n_tiles, (units + G - 1) / G);
     kern<<<grid, kBwdThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
     return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
 }
