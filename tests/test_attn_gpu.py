@@ -166,6 +166,30 @@ def test_forward_head_groups_with_a_partial_last_group():
     assert st == U.OK, hex(word)
 
 
+def test_backward_unit_groups_with_a_partial_last_group():
+    """Short causal sequences run the backward's grouped order (G units per grid row: 2 at
+    L = 16384, d_h = 128). With 3 heads the last group is partial and its spare CTAs leave at
+    once. Each head's dK and dV must equal, bit for bit, the same head run alone (one unit: the
+    plain kernel), and its dQ must agree up to the order of the fp32 additions."""
+    B, L, H, d, P = 1, 16384, 3, 128, 1
+    g = torch.Generator().manual_seed(22)
+    x = {n: torch.randn((P, B, L, H, d), generator=g).mul_(0.5).to(torch.bfloat16).cuda()
+         for n in ("q", "k", "v", "do")}
+    mask = U.Mask.causal()
+    o, lse = U.attn_fwd(x["q"], x["k"], x["v"], P, mask)
+    dq, dk, dv = U.attn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], P, mask)
+    for h in range(H):
+        one = {n: t[:, :, :, h:h + 1, :].contiguous() for n, t in x.items()}
+        o1, lse1 = U.attn_fwd(one["q"], one["k"], one["v"], P, mask)
+        dq1, dk1, dv1 = U.attn_bwd(one["q"], one["k"], one["v"], o1, lse1, one["do"], P, mask)
+        assert torch.equal(dk[:, :, :, h:h + 1, :].view(torch.int16), dk1.view(torch.int16)), h
+        assert torch.equal(dv[:, :, :, h:h + 1, :].view(torch.int16), dv1.view(torch.int16)), h
+        err = (dq[:, :, :, h:h + 1, :].float() - dq1.float()).abs().max().item()
+        assert err <= 2e-2, (h, err)
+    st, word = U.device_status()
+    assert st == U.OK, hex(word)
+
+
 def test_repeat_runs_are_deterministic_except_dq():
     w = workloads.Workload("rep", 1, 1024, 4, 128, 4, "causal", True, 5)
     t = {n: x.cuda() for n, x in workloads.draw_workload(w).items()}
