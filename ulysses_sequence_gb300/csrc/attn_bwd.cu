@@ -338,7 +338,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(q_full + i, 1);
+            mbar_init(q_full + i, 2);
             mbar_init(q_empty + i, 1);
         }
         mbar_init(do_full, 1);
@@ -389,7 +389,19 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int h = u.h_first + ih;
                 const int q0 = bwd_q_step<MASK>(p, q_first, it - ih * n_per) * kQStep;
                 const bool whole = bulk_stats && q0 + kQStep <= p.L;
-                if (!whole) {
+                // Q by TMA; lse and Delta by the warp's lanes (two 16-byte loads each, both in
+                // flight before either store), so that the TMA queue carries two instructions
+                // per Q tile instead of four. The slot's barrier takes both arrivals.
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(q_full + qs, C::T_BYTES);
+                    bwd_load<D>(sQ + qs * C::T_BYTES, &tm_q, q_full + qs, p, q0, h, b);
+                }
+                if (whole) {
+                    const float4 l4 = reinterpret_cast<const float4*>(p.lse + stat_index(p, q0, h, b))[lane];
+                    const float4 d4 = reinterpret_cast<const float4*>(p.delta + stat_index(p, q0, h, b))[lane];
+                    reinterpret_cast<float4*>(sLSE + qs * kQStep)[lane] = l4;
+                    reinterpret_cast<float4*>(sDelta + qs * kQStep)[lane] = d4;
+                } else {
                     for (int c = lane; c < kQStep; c += 32) {
                         const int q = q0 + c;
                         const bool in = q < p.L;
@@ -397,16 +409,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         sLSE[qs * kQStep + c] = in ? p.lse[stat_index(p, q, h, b)] : INFINITY;
                         sDelta[qs * kQStep + c] = in ? p.delta[stat_index(p, q, h, b)] : 0.f;
                     }
-                    __syncwarp();
                 }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(q_full + qs, C::T_BYTES + (whole ? 2 * kQStep * 4 : 0));
-                    if (whole) {
-                        bulk_load(sLSE + qs * kQStep, p.lse + stat_index(p, q0, h, b), kQStep * 4, q_full + qs);
-                        bulk_load(sDelta + qs * kQStep, p.delta + stat_index(p, q0, h, b), kQStep * 4, q_full + qs);
-                    }
-                    bwd_load<D>(sQ + qs * C::T_BYTES, &tm_q, q_full + qs, p, q0, h, b);
-                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(q_full + qs);
                 ++nq;
                 if (it >= 1) {
                     ok = __all_sync(0xffffffffu, mbar_wait(do_empty, (it - 1) & 1, ab, ROLE_LOAD, 2));
