@@ -340,7 +340,9 @@ def run_distributed(args, w, world, rank, local):
         h2d = sum(v.numel() * v.element_size() for v in host.values())
         d2h = sum(h.numel() * h.element_size() for h in out_host)
         comm = w.B * w.L * (2 * w.H + 2 * w.Hkv) * w.d * 2 // world  # Q, K, V in and O out, bf16, per rank
-        kernels = (4 * w.B + 1) + ((4 * w.B + 3) if w.backward else 0)
+        # packs and unpacks per batch row, the attention calls (the backward's prep, main and convert
+        # kernels, plus the two schedule kernels for a block-sparse mask)
+        kernels = (4 * w.B + 1) + ((4 * w.B + 3 + (2 if w.mask == "block_sparse" else 0)) if w.backward else 0)
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "strong",
@@ -718,7 +720,9 @@ def main():
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "overlap": "steps alternate two device buffer sets on two streams; copies of one step "
                                "overlap kernels of another"},
-            "gpu_launches": args.steps * (1 + (3 if w.backward else 0)),
+            # per step: the forward; the backward call's Delta prep, main kernel and dQ convert,
+            # plus the two block-sparse schedule kernels for that mask
+            "gpu_launches": args.steps * (1 + ((3 + (2 if w.mask == "block_sparse" else 0)) if w.backward else 0)),
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
