@@ -17,8 +17,9 @@
 // leader, reads both CTAs' shared memory and writes each CTA's 128 rows into its own tensor
 // memory. Per SM that halves the B operand's loads and shared-memory reads against a 1-SM
 // 128 x 256 tile, whose traffic (about 190 B/clk) exceeded the 128 B/clk shared-memory port.
-//   warp 0 (both CTAs) loads A and B K-slices of 64 through a 6-stage TMA ring that runs on
-//          across tiles; both CTAs' loads count on the leader's barrier;
+//   warp 0 (both CTAs) loads A and B K-slices of 128 through a 3-stage TMA ring that runs on
+//          across tiles, one copy per operand and slice (both 64-wide chunks: the per-SM TMA
+//          engine moves larger copies faster); both CTAs' loads count on the leader's barrier;
 //   warp 1 (leader) issues the MMAs into one of two TMEM accumulators (256 columns each) and
 //          commits to the barriers of both CTAs at once;
 //   warps 2-5 (both CTAs) convert the other accumulator to bf16 and store their rows, so a
@@ -34,10 +35,12 @@ namespace ulysses {
 
 struct GemmCfg {
     // a CTA pair computes a 256 x 256 tile; each CTA holds 128 rows of A and 128 rows of B
-    static constexpr int BM = 128, BN = 256, BK = 64, STAGES = 6, GROUP_M = 8;
+    // K-slices of 128: one TMA copy brings both 64-wide chunks of a 128-row slice (32 KB)
+    static constexpr int BM = 128, BN = 256, BK = 128, STAGES = 3, GROUP_M = 8;
     static constexpr int PM = 2 * BM;                  // pair tile rows
-    static constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
-    static constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's half of B
+    static constexpr uint32_t CHUNK = 128 * 128;       // 128 rows x 64 elements, swizzled
+    static constexpr uint32_t A_BYTES = BM * BK * 2;   // 32 KB
+    static constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;  // 32 KB: this CTA's half of B
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t OFF_BAR = STAGES * STAGE_BYTES;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
@@ -125,8 +128,8 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                     // both CTAs' bytes count on the leader's barrier; the leader expects them all
                     if (rank == 0) mbar_arrive_expect_tx(full + s, 2 * C::STAGE_BYTES);
                     const uint32_t lbar = cluster_addr(full + s, 0);
-                    tma_load_2d_pair(st, &tm_a, lbar, ks * C::BK, m0 + int(rank) * C::BM);
-                    tma_load_2d_pair(st + C::A_BYTES, &tm_b, lbar, ks * C::BK, n0 + int(rank) * (C::BN / 2));
+                    tma_load_5d_pair(st, &tm_a, lbar, 0, m0 + int(rank) * C::BM, ks * (C::BK / 64), 0, 0);
+                    tma_load_5d_pair(st + C::A_BYTES, &tm_b, lbar, 0, n0 + int(rank) * (C::BN / 2), ks * (C::BK / 64), 0, 0);
                 }
             }
             if (!ok) {
@@ -160,8 +163,10 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                     const uint64_t da = sdesc_sw128(base + s * C::STAGE_BYTES, 16, 1024);
                     const uint64_t db = sdesc_sw128(base + s * C::STAGE_BYTES + C::A_BYTES, 16, 1024);
 #pragma unroll
-                    for (int k = 0; k < C::BK / 16; ++k)
-                        umma_pair_ss(acc, sdesc_add(da, k * 32), sdesc_add(db, k * 32), idesc, (ks > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < C::BK / 16; ++k) {
+                        const uint32_t o = (k >> 2) * C::CHUNK + (k & 3) * 32;
+                        umma_pair_ss(acc, sdesc_add(da, o), sdesc_add(db, o), idesc, (ks > 0 || k > 0) ? 1u : 0u);
+                    }
                     umma_pair_commit_both(empty + s);
                 }
                 if (ok) umma_pair_commit_both(acc_full + a);
@@ -224,11 +229,13 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
 // 2-D bf16 tensor map over a row-major [rows][cols] matrix with a (64, box_rows) box and the
 // 128-byte swizzle, zero fill out of bounds.
 static bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {64, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return encode_tensor_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr);
+    // (64 elements, rows, 64-wide column chunks, 1, 1): one box is box_rows rows of two chunks,
+    // chunk after chunk; a chunk past the last column reads zeros
+    cuuint64_t dims[5] = {64, rows, (cols + 63) / 64, 1, 1};
+    cuuint64_t strides[4] = {cols * 2, 128, cols * 2 * rows, cols * 2 * rows};
+    cuuint32_t box[5] = {64, box_rows, 2, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return encode_tensor_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, estr);
 }
 
 int launch_proj_gemm(int M, int N, int K, const void* a, const void* b, int n_out, const int* col0, void* const* out,
