@@ -31,7 +31,10 @@ def _bits(t):
 
 # P, B, L, H, H_kv, d, hidden: whole tiles; ragged rows (M = 400), ragged K (hidden 96) and
 # columns (N = 6 heads of 64 = 384 = 1.5 tiles); grouped heads with d = 128
-CASES = [(2, 1, 256, 4, 4, 64, 256), (4, 2, 200, 4, 1, 64, 96), (4, 1, 512, 8, 2, 128, 1024)]
+# hidden sizes: whole 128-wide K slices (256, 1024), an odd number of 64-wide chunks (320: the last
+# slice's second chunk reads zeros) and a ragged K (96: 2-D boxes with zero fill past column 96)
+CASES = [(2, 1, 256, 4, 4, 64, 256), (4, 2, 200, 4, 1, 64, 96), (4, 1, 512, 8, 2, 128, 1024),
+         (2, 1, 256, 4, 2, 64, 320)]
 
 
 @pytest.mark.parametrize("P,B,L,H,Hkv,d,hidden", CASES)

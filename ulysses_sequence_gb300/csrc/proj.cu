@@ -54,6 +54,7 @@ struct GemmParams {
     int col0[4];        // range i is columns [col0[i], col0[i + 1])
     void* out[3];       // bf16, row-major
     int ld[3];          // row pitch of each output in elements
+    int chunked;        // 1: the maps bring a whole 128-wide K slice per copy (K % 64 == 0)
     uint32_t* err;
 };
 
@@ -128,8 +129,17 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                     // both CTAs' bytes count on the leader's barrier; the leader expects them all
                     if (rank == 0) mbar_arrive_expect_tx(full + s, 2 * C::STAGE_BYTES);
                     const uint32_t lbar = cluster_addr(full + s, 0);
-                    tma_load_5d_pair(st, &tm_a, lbar, 0, m0 + int(rank) * C::BM, ks * (C::BK / 64), 0, 0);
-                    tma_load_5d_pair(st + C::A_BYTES, &tm_b, lbar, 0, n0 + int(rank) * (C::BN / 2), ks * (C::BK / 64), 0, 0);
+                    const int ra = m0 + int(rank) * C::BM, rb = n0 + int(rank) * (C::BN / 2);
+                    if (p.chunked) {
+                        tma_load_5d_pair(st, &tm_a, lbar, 0, ra, ks * (C::BK / 64), 0, 0);
+                        tma_load_5d_pair(st + C::A_BYTES, &tm_b, lbar, 0, rb, ks * (C::BK / 64), 0, 0);
+                    } else {
+                        // a ragged K: 2-D boxes, whose columns past K read zeros
+                        for (int c = 0; c < C::BK / 64; ++c) {
+                            tma_load_2d_pair(st + c * C::CHUNK, &tm_a, lbar, ks * C::BK + c * 64, ra);
+                            tma_load_2d_pair(st + C::A_BYTES + c * C::CHUNK, &tm_b, lbar, ks * C::BK + c * 64, rb);
+                        }
+                    }
                 }
             }
             if (!ok) {
@@ -228,14 +238,23 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
 
 // 2-D bf16 tensor map over a row-major [rows][cols] matrix with a (64, box_rows) box and the
 // 128-byte swizzle, zero fill out of bounds.
-static bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-    // (64 elements, rows, 64-wide column chunks, 1, 1): one box is box_rows rows of two chunks,
-    // chunk after chunk; a chunk past the last column reads zeros
-    cuuint64_t dims[5] = {64, rows, (cols + 63) / 64, 1, 1};
-    cuuint64_t strides[4] = {cols * 2, 128, cols * 2 * rows, cols * 2 * rows};
-    cuuint32_t box[5] = {64, box_rows, 2, 1, 1};
-    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    return encode_tensor_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, estr);
+// Tensor map over a row-major [rows][cols] bf16 matrix, 128-byte swizzle, zero fill out of bounds.
+// chunked (cols % 64 == 0): 5-D (64 elements, rows, 64-wide column chunks, 1, 1) with a box of
+// box_rows rows of two chunks, chunk after chunk, so that one copy brings a 128-wide K slice (a
+// chunk past the last column reads zeros). Otherwise 2-D (cols, rows) with a (64, box_rows) box.
+static bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, bool chunked) {
+    if (chunked) {
+        cuuint64_t dims[5] = {64, rows, cols / 64, 1, 1};
+        cuuint64_t strides[4] = {cols * 2, 128, cols * 2 * rows, cols * 2 * rows};
+        cuuint32_t box[5] = {64, box_rows, 2, 1, 1};
+        cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        return encode_tensor_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, estr);
+    }
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return encode_tensor_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr);
 }
 
 int launch_proj_gemm(int M, int N, int K, const void* a, const void* b, int n_out, const int* col0, void* const* out,
@@ -249,7 +268,9 @@ int launch_proj_gemm(int M, int N, int K, const void* a, const void* b, int n_ou
     if (!p.err) return ULYSSES_ERR_CUDA;
     CUtensorMap ma, mb;
     // each CTA of a pair loads 128 rows of A and 128 rows (its half) of B per K-slice
-    if (!encode_2d(&ma, a, uint64_t(M), uint64_t(K), C::BM) || !encode_2d(&mb, b, uint64_t(N), uint64_t(K), C::BN / 2))
+    p.chunked = K % 64 == 0 ? 1 : 0;
+    if (!encode_2d(&ma, a, uint64_t(M), uint64_t(K), C::BM, p.chunked) ||
+        !encode_2d(&mb, b, uint64_t(N), uint64_t(K), C::BN / 2, p.chunked))
         return ULYSSES_ERR_CUDA;
     if (!set_max_dynamic_smem(reinterpret_cast<const void*>(proj_gemm_kernel), C::SMEM_BYTES)) return ULYSSES_ERR_CUDA;
     const int tiles = ((M + C::PM - 1) / C::PM) * ((N + C::BN - 1) / C::BN);
