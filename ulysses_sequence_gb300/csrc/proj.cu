@@ -24,8 +24,8 @@
 //          commits to the barriers of both CTAs at once;
 //   warps 2-5 (both CTAs) convert the other accumulator to bf16 and store their rows, so a
 //          tile's epilogue overlaps the next tile's MMAs.
-// Tiles are rasterized in groups of 8 row tiles, so the tiles in flight at one time share
-// their A and B slices in L2.
+// Tiles are rasterized in groups of 8 row tiles (16 when B exceeds 48 MB), so the tiles in
+// flight at one time share their A and B slices in L2.
 #include <mutex>
 
 #include "common.cuh"
@@ -36,7 +36,7 @@ namespace ulysses {
 struct GemmCfg {
     // a CTA pair computes a 256 x 256 tile; each CTA holds 128 rows of A and 128 rows of B
     // K-slices of 128: one TMA copy brings both 64-wide chunks of a 128-row slice (32 KB)
-    static constexpr int BM = 128, BN = 256, BK = 128, STAGES = 3, GROUP_M = 8;
+    static constexpr int BM = 128, BN = 256, BK = 128, STAGES = 3;
     static constexpr int PM = 2 * BM;                  // pair tile rows
     static constexpr uint32_t CHUNK = 128 * 128;       // 128 rows x 64 elements, swizzled
     static constexpr uint32_t A_BYTES = BM * BK * 2;   // 32 KB
@@ -55,6 +55,7 @@ struct GemmParams {
     void* out[3];       // bf16, row-major
     int ld[3];          // row pitch of each output in elements
     int chunked;        // 1: the maps bring a whole 128-wide K slice per copy (K % 64 == 0)
+    int group_m;        // row tiles per raster group
     uint32_t* err;
 };
 
@@ -79,13 +80,13 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     const int tiles_m = (p.M + C::PM - 1) / C::PM, tiles_n = (p.N + C::BN - 1) / C::BN;
     const int n_tiles = tiles_m * tiles_n;
     const int n_k = (p.K + C::BK - 1) / C::BK;
-    // grouped raster: GROUP_M row tiles vary fastest, then column tiles, then groups
+    // grouped raster: group_m row tiles vary fastest, then column tiles, then groups
     auto tile_origin = [&](int t, int& m0, int& n0) {
-        const int per_group = C::GROUP_M * tiles_n;
+        const int per_group = p.group_m * tiles_n;
         const int group = t / per_group;
-        const int gm = min(C::GROUP_M, tiles_m - group * C::GROUP_M);  // row tiles in this group
+        const int gm = min(p.group_m, tiles_m - group * p.group_m);  // row tiles in this group
         const int in_group = t - group * per_group;
-        m0 = (group * C::GROUP_M + in_group % gm) * C::PM;
+        m0 = (group * p.group_m + in_group % gm) * C::PM;
         n0 = (in_group / gm) * C::BN;
     };
 
@@ -269,6 +270,8 @@ int launch_proj_gemm(int M, int N, int K, const void* a, const void* b, int n_ou
     CUtensorMap ma, mb;
     // each CTA of a pair loads 128 rows of A and 128 rows (its half) of B per K-slice
     p.chunked = K % 64 == 0 ? 1 : 0;
+    // every raster group reads all of B: when B is large, taller groups read it fewer times
+    p.group_m = size_t(N) * size_t(K) * 2 > (size_t(48) << 20) ? 16 : 8;
     if (!encode_2d(&ma, a, uint64_t(M), uint64_t(K), C::BM, p.chunked) ||
         !encode_2d(&mb, b, uint64_t(N), uint64_t(K), C::BN / 2, p.chunked))
         return ULYSSES_ERR_CUDA;
