@@ -494,31 +494,72 @@ def main():
     ms_per_step = elapsed_ms / args.steps
     value = total_flops * world * args.steps / (elapsed_ms * 1e-3) / 1e12
 
-    # ---- end to end through the public API with host buffers (pinned). Consecutive steps
-    # alternate between two device buffer sets, each on its own stream, so that one step's
-    # host<->device copies overlap another step's kernels, as a training loop that streams its
-    # inputs would run. Every step still copies its own inputs in and its results out inside
-    # the timed region.
-    out_names = ("o", "dq", "dk", "dv", "lse")
+    # ---- end to end through the public API with host buffers (pinned). A training loop that
+    # streams its inputs runs three streams: copies in, kernels, copies out. Consecutive steps
+    # alternate between two device buffer sets, so that one step's copies run under another
+    # step's kernels. Within a step Q, K, V go in first and the forward waits for them only;
+    # dO follows while the forward runs; O and lse go out while the backward runs, dQ, dK, dV
+    # after it. Events order the reuse of a buffer set: its inputs are overwritten only after
+    # the kernels of the step two back have read them, its outputs only after they were copied
+    # out. Every step still copies its own inputs in and its results out inside the timed region.
+    out_fwd, out_bwd = ("o", "lse"), (("dq", "dk", "dv") if w.backward else ())
     sets = [{"x": x, "o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv, "ws": ws},
             {"x": {n: torch.empty_like(v) for n, v in x.items()}, "o": torch.empty_like(o),
              "lse": torch.empty_like(lse), "dq": torch.empty_like(dq), "dk": torch.empty_like(dk),
              "dv": torch.empty_like(dv), "ws": torch.empty_like(ws)}]
-    host_out = [{n: torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype, pin_memory=True) for n in out_names}
-                for _ in range(2)]
-    e2e_streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    host_out = [{n: torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype, pin_memory=True)
+                 for n in out_fwd + out_bwd} for _ in range(2)]
+    s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    # per buffer set, created once and recorded again each step (a wait takes the record made
+    # before it): inputs in, forward done, kernels done (its inputs read), outputs copied out
+    names = ("qkv_in", "do_in", "fwd_done", "run_done", "fwd_out", "bwd_out")
+    evs = [{n: torch.cuda.Event() for n in names} for _ in range(2)]
+    # the kernels' own time in each step, beside the copies (timing events on the kernel stream)
+    k_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(max(2, args.steps))]
 
     def e2e_step(i):
-        b, st = sets[i % 2], e2e_streams[i % 2]
-        with torch.cuda.stream(st):
-            for n in ("q", "k", "v", "do"):
+        k = i % 2
+        b, e = sets[k], evs[k]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(e["run_done"])
+            for n in ("q", "k", "v"):
                 b["x"][n].copy_(host[n], non_blocking=True)
-            U.attn_fwd(b["x"]["q"], b["x"]["k"], b["x"]["v"], w.P, mask, o=b["o"], lse=b["lse"], stream=st)
+            e["qkv_in"].record(s_in)
             if w.backward:
+                b["x"]["do"].copy_(host["do"], non_blocking=True)
+                e["do_in"].record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(e["qkv_in"])
+            if i >= 2:
+                s_run.wait_event(e["fwd_out"])
+            k_ev[i][0].record(s_run)
+            U.attn_fwd(b["x"]["q"], b["x"]["k"], b["x"]["v"], w.P, mask, o=b["o"], lse=b["lse"], stream=s_run)
+            e["fwd_done"].record(s_run)
+            if w.backward:
+                s_run.wait_event(e["do_in"])
+                if i >= 2:
+                    s_run.wait_event(e["bwd_out"])
                 U.attn_bwd(b["x"]["q"], b["x"]["k"], b["x"]["v"], b["o"], b["lse"], b["x"]["do"], w.P, mask,
-                           dq=b["dq"], dk=b["dk"], dv=b["dv"], workspace=b["ws"], stream=st)
-            for n in out_names:
-                host_out[i % 2][n].copy_(b[n], non_blocking=True)
+                           dq=b["dq"], dk=b["dk"], dv=b["dv"], workspace=b["ws"], stream=s_run)
+            e["run_done"].record(s_run)
+            k_ev[i][1].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(e["fwd_done"])
+            for n in out_fwd:
+                host_out[k][n].copy_(b[n], non_blocking=True)
+            e["fwd_out"].record(s_out)
+            if out_bwd:
+                s_out.wait_event(e["run_done"])
+                for n in out_bwd:
+                    host_out[k][n].copy_(b[n], non_blocking=True)
+                e["bwd_out"].record(s_out)
+
+    def mark(st):
+        done = torch.cuda.Event()
+        done.record(st)
+        return done
 
     e2e_step(0)
     e2e_step(1)
@@ -528,18 +569,18 @@ def main():
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
-    for st in e2e_streams:
+    for st in (s_in, s_run, s_out):
         st.wait_event(e_start)
     for i in range(n_e2e):
         e2e_step(i)
-    for st in e2e_streams:
-        done = torch.cuda.Event()
-        done.record(st)
-        stream.wait_event(done)
+    for st in (s_in, s_run, s_out):
+        stream.wait_event(mark(st))
     e_end.record(stream)
     e_end.synchronize()
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / n_e2e, world)
-    h2d = sum(host[n].numel() * host[n].element_size() for n in ("q", "k", "v", "do"))
+    e2e_kernel_ms = sum(a.elapsed_time(b) for a, b in k_ev[:n_e2e]) / n_e2e
+    in_names = ("q", "k", "v", "do") if w.backward else ("q", "k", "v")
+    h2d = sum(host[n].numel() * host[n].element_size() for n in in_names)
     d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
     st_e2e, word_e2e = U.device_status()
     U.check(st_e2e, f"device status after the end-to-end steps ({word_e2e:#x})")
@@ -718,8 +759,10 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": total_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "overlap": "steps alternate two device buffer sets on two streams; copies of one step "
-                               "overlap kernels of another"},
+                    "kernel_ms_per_step": e2e_kernel_ms,
+                    "overlap": "copies in, kernels and copies out on three streams over two device buffer "
+                               "sets: one step's copies run under another step's kernels; dO in under the "
+                               "forward, O and lse out under the backward"},
             # per step: the forward; the backward call's Delta prep, main kernel and dQ convert,
             # plus the two block-sparse schedule kernels for that mask
             "gpu_launches": args.steps * (1 + ((3 + (2 if w.mask == "block_sparse" else 0)) if w.backward else 0)),
