@@ -12,9 +12,14 @@ timed beside it in HBM GB/s (2 bytes read + 2 written per element).
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
 
+The line's e2e figure runs the same steps through the public calls with every step's inputs
+copied in from pinned host memory and its results copied out, pipelined over three streams
+(copies in, kernels, copies out) and two device buffer sets.
+
 With --impl reference the CPU oracle is timed instead, on a bounded sample of rows.
-Under torchrun each rank runs its own replica (the path has no cross-rank exchange on
-one GPU); rank 0 prints one JSON line with the whole-job value.
+Under torchrun (N > 1) the processes are real Ulysses ranks: each owns L/N tokens on its own
+GPU, the all-to-alls run through NCCL, and rank 0 prints one JSON line with the whole-job
+value (strong scaling: the total work is the one layer's). --dist runs that path on one GPU.
 """
 
 from __future__ import annotations
