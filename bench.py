@@ -388,6 +388,85 @@ def cuda_events_time(fn, stream, iters):
     return start.elapsed_time(end) / iters
 
 
+def e2e_pipeline(U, w, mask, host_in, sets, host_out, steps, stream):
+    """Run `steps` forward(+backward) steps through the public calls, each copying its inputs in
+    from pinned host memory and its results out, as a training loop that streams its inputs
+    would: three streams (copies in, kernels, copies out) over two device buffer sets, so that
+    one step's copies run under another step's kernels. Within a step Q, K, V go in first and
+    the forward waits for them alone; dO follows under the forward; O and lse go out under the
+    backward, dQ, dK and dV after it. Events order the reuse of a buffer set: its inputs are
+    overwritten only once the kernels of the step two back have read them, and its outputs
+    only once they were copied out.
+
+    Step i reads host_in[i % len(host_in)] and writes host_out[i % len(host_out)]. Returns the
+    elapsed ms of all steps (events on `stream`, which every stream joins at both ends) and the
+    kernel stream's own mean ms per step."""
+    out_fwd, out_bwd = ("o", "lse"), (("dq", "dk", "dv") if w.backward else ())
+    dev = sets[0]["o"].device
+    s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    # per buffer set, created once and recorded again each step (a wait takes the record made
+    # before it): inputs in, forward done, kernels done (its inputs read), outputs copied out
+    names = ("qkv_in", "do_in", "fwd_done", "run_done", "fwd_out", "bwd_out")
+    evs = [{n: torch.cuda.Event() for n in names} for _ in range(2)]
+    k_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+
+    def one(i):
+        k = i % 2
+        b, e = sets[k], evs[k]
+        hin, hout = host_in[i % len(host_in)], host_out[i % len(host_out)]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(e["run_done"])
+            for n in ("q", "k", "v"):
+                b["x"][n].copy_(hin[n], non_blocking=True)
+            e["qkv_in"].record(s_in)
+            if w.backward:
+                b["x"]["do"].copy_(hin["do"], non_blocking=True)
+                e["do_in"].record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(e["qkv_in"])
+            if i >= 2:
+                s_run.wait_event(e["fwd_out"])
+            k_ev[i][0].record(s_run)
+            U.attn_fwd(b["x"]["q"], b["x"]["k"], b["x"]["v"], w.P, mask, o=b["o"], lse=b["lse"], stream=s_run)
+            e["fwd_done"].record(s_run)
+            if w.backward:
+                s_run.wait_event(e["do_in"])
+                if i >= 2:
+                    s_run.wait_event(e["bwd_out"])
+                U.attn_bwd(b["x"]["q"], b["x"]["k"], b["x"]["v"], b["o"], b["lse"], b["x"]["do"], w.P, mask,
+                           dq=b["dq"], dk=b["dk"], dv=b["dv"], workspace=b["ws"], stream=s_run)
+            e["run_done"].record(s_run)
+            k_ev[i][1].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(e["fwd_done"])
+            for n in out_fwd:
+                hout[n].copy_(b[n], non_blocking=True)
+            e["fwd_out"].record(s_out)
+            if out_bwd:
+                s_out.wait_event(e["run_done"])
+                for n in out_bwd:
+                    hout[n].copy_(b[n], non_blocking=True)
+                e["bwd_out"].record(s_out)
+
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for st in (s_in, s_run, s_out):
+        st.wait_event(start)
+    for i in range(steps):
+        one(i)
+    for st in (s_in, s_run, s_out):
+        done = torch.cuda.Event()
+        done.record(st)
+        stream.wait_event(done)
+    end.record(stream)
+    end.synchronize()
+    kernel_ms = sum(a.elapsed_time(b) for a, b in k_ev) / steps
+    return start.elapsed_time(end), kernel_ms
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -499,97 +578,26 @@ def main():
     ms_per_step = elapsed_ms / args.steps
     value = total_flops * world * args.steps / (elapsed_ms * 1e-3) / 1e12
 
-    # ---- end to end through the public API with host buffers (pinned). A training loop that
-    # streams its inputs runs three streams: copies in, kernels, copies out. Consecutive steps
-    # alternate between two device buffer sets, so that one step's copies run under another
-    # step's kernels. Within a step Q, K, V go in first and the forward waits for them only;
-    # dO follows while the forward runs; O and lse go out while the backward runs, dQ, dK, dV
-    # after it. Events order the reuse of a buffer set: its inputs are overwritten only after
-    # the kernels of the step two back have read them, its outputs only after they were copied
-    # out. Every step still copies its own inputs in and its results out inside the timed region.
-    out_fwd, out_bwd = ("o", "lse"), (("dq", "dk", "dv") if w.backward else ())
+    # ---- end to end through the public API with host buffers (pinned), pipelined (e2e_pipeline)
     sets = [{"x": x, "o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv, "ws": ws},
             {"x": {n: torch.empty_like(v) for n, v in x.items()}, "o": torch.empty_like(o),
              "lse": torch.empty_like(lse), "dq": torch.empty_like(dq), "dk": torch.empty_like(dk),
              "dv": torch.empty_like(dv), "ws": torch.empty_like(ws)}]
-    host_out = [{n: torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype, pin_memory=True)
-                 for n in out_fwd + out_bwd} for _ in range(2)]
-    s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
-    # per buffer set, created once and recorded again each step (a wait takes the record made
-    # before it): inputs in, forward done, kernels done (its inputs read), outputs copied out
-    names = ("qkv_in", "do_in", "fwd_done", "run_done", "fwd_out", "bwd_out")
-    evs = [{n: torch.cuda.Event() for n in names} for _ in range(2)]
-    # the kernels' own time in each step, beside the copies (timing events on the kernel stream)
-    k_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(max(2, args.steps))]
-
-    def e2e_step(i):
-        k = i % 2
-        b, e = sets[k], evs[k]
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(e["run_done"])
-            for n in ("q", "k", "v"):
-                b["x"][n].copy_(host[n], non_blocking=True)
-            e["qkv_in"].record(s_in)
-            if w.backward:
-                b["x"]["do"].copy_(host["do"], non_blocking=True)
-                e["do_in"].record(s_in)
-        with torch.cuda.stream(s_run):
-            s_run.wait_event(e["qkv_in"])
-            if i >= 2:
-                s_run.wait_event(e["fwd_out"])
-            k_ev[i][0].record(s_run)
-            U.attn_fwd(b["x"]["q"], b["x"]["k"], b["x"]["v"], w.P, mask, o=b["o"], lse=b["lse"], stream=s_run)
-            e["fwd_done"].record(s_run)
-            if w.backward:
-                s_run.wait_event(e["do_in"])
-                if i >= 2:
-                    s_run.wait_event(e["bwd_out"])
-                U.attn_bwd(b["x"]["q"], b["x"]["k"], b["x"]["v"], b["o"], b["lse"], b["x"]["do"], w.P, mask,
-                           dq=b["dq"], dk=b["dk"], dv=b["dv"], workspace=b["ws"], stream=s_run)
-            e["run_done"].record(s_run)
-            k_ev[i][1].record(s_run)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(e["fwd_done"])
-            for n in out_fwd:
-                host_out[k][n].copy_(b[n], non_blocking=True)
-            e["fwd_out"].record(s_out)
-            if out_bwd:
-                s_out.wait_event(e["run_done"])
-                for n in out_bwd:
-                    host_out[k][n].copy_(b[n], non_blocking=True)
-                e["bwd_out"].record(s_out)
-
-    def mark(st):
-        done = torch.cuda.Event()
-        done.record(st)
-        return done
-
-    e2e_step(0)
-    e2e_step(1)
-    torch.cuda.synchronize()
+    out_names = ("o", "lse") + (("dq", "dk", "dv") if w.backward else ())
+    host_out = [{n: torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype, pin_memory=True) for n in out_names}
+                for _ in range(2)]
+    e2e_pipeline(U, w, mask, [host], sets, host_out, 2, stream)  # warm-up
     barrier(world)
     n_e2e = max(2, args.steps)
-    e_start = torch.cuda.Event(enable_timing=True)
-    e_end = torch.cuda.Event(enable_timing=True)
-    e_start.record(stream)
-    for st in (s_in, s_run, s_out):
-        st.wait_event(e_start)
-    for i in range(n_e2e):
-        e2e_step(i)
-    for st in (s_in, s_run, s_out):
-        stream.wait_event(mark(st))
-    e_end.record(stream)
-    e_end.synchronize()
-    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / n_e2e, world)
-    e2e_kernel_ms = sum(a.elapsed_time(b) for a, b in k_ev[:n_e2e]) / n_e2e
-    in_names = ("q", "k", "v", "do") if w.backward else ("q", "k", "v")
-    h2d = sum(host[n].numel() * host[n].element_size() for n in in_names)
-    d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
+    e2e_elapsed, e2e_kernel_ms = e2e_pipeline(U, w, mask, [host], sets, host_out, n_e2e, stream)
+    e2e_ms = max_over_ranks(e2e_elapsed / n_e2e, world)
     st_e2e, word_e2e = U.device_status()
     U.check(st_e2e, f"device status after the end-to-end steps ({word_e2e:#x})")
     del sets[1]
+
+    in_names = ("q", "k", "v", "do") if w.backward else ("q", "k", "v")
+    h2d = sum(host[n].numel() * host[n].element_size() for n in in_names)
+    d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
 
     # ---- standalone relayout (seq->head of one tensor), HBM bound; launched through the raw
     # C call with prepared arguments so the host side keeps ahead of the ~80 us kernel
